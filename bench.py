@@ -1,0 +1,496 @@
+"""Benchmark of the fused gated group-RMSNorm on GB300.
+
+Prints ONE JSON line (rank 0).  A step is one call of the whole operation
+(validate, select, one kernel: load y/gate, gate, group reduction,
+normaliser, epilogue, store) over one batch of synthetic input.  Default
+workload: the Mamba-2 prefill shape (4096 rows x 7680, groups of 960, bf16).
+
+  value      algorithmic HBM GB/s (y + gate read once, out written once, the
+             weight once) / device time of the K timed steps, summed over ranks
+  e2e        the same metric through the public Python API with pinned HOST
+             buffers: host->device copy of y and gate, the call, device->host
+             copy of out, every step
+  roofline   the kernel's achieved GB/s against the measured HBM copy peak;
+             traffic = DRAM bytes per launch from the ncu capture recorded in
+             profiles/dram_traffic.txt (null when the kernels changed since)
+  cpu_baseline  the single-threaded CPU oracle on a bounded sample
+
+Timing: W warm-up steps, then K steps between two CUDA events on the
+launching stream with a barrier and a synchronize on both sides, max over
+ranks.  Inputs rotate over several copies whose total exceeds the L2, so
+every step reads y and gate from HBM.
+
+--impl reference times the CPU oracle instead (the reference arm of this
+build): same metric and workload, each step a bounded sample of rows.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import ggrn_inputs  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and rows/s; decode µs/call"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+CSRC = os.path.join(ROOT, "gated_group_rmsnorm_gb300", "csrc")
+IO_DTYPE = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (host logic; tested with gloo ranks on CPU).
+# ---------------------------------------------------------------------------
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, device) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier() -> None:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(bytes_per_step: int, rows_per_step: int, steps: int, max_ms: float,
+              world: int) -> dict:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    secs = max_ms / 1e3
+    return {"gbs": world * steps * bytes_per_step / secs / 1e9,
+            "rows_per_s": world * steps * rows_per_step / secs,
+            "ms_per_step": max_ms / steps}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str, period_ms: int = 50):
+        self.uuid = uuid.replace("GPU-", "").lower()
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9 and parts[0].replace("GPU-", "").lower() == self.uuid:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(win) < 3:  # short timed region: widen to the samples around it
+            win = [p for t, p in self.samples if t0 - 1.0 <= t <= t1 + 0.2]
+            window = "timed+1s before"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none (nvidia-smi unavailable)"}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        reasons = sorted({r for p in win for r, v in zip(self.REASONS, p[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# Roofline denominators and recorded ncu traffic.
+# ---------------------------------------------------------------------------
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, fn), "rb") as fh:
+                h.update(fn.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str) -> tuple[float | None, str]:
+    """DRAM bytes per launch from profiles/dram_traffic.txt, if it was captured
+    on the current kernel sources (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no capture recorded"
+    cur = kernel_source_hash()
+    found = None
+    with open(TRAFFIC_FILE) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if kv.get("workload") == workload:
+                found = kv
+    if found is None:
+        return None, "no capture for this workload"
+    if found.get("csrc_sha") != cur:
+        return None, f"kernels changed since the capture ({found.get('csrc_sha')} != {cur})"
+    return float(found["dram_bytes_per_launch"]), found.get("note", "ncu capture")
+
+
+# ---------------------------------------------------------------------------
+# Our arm.
+# ---------------------------------------------------------------------------
+def _raw_args(g, inp, out, wl, stream_handle):
+    """Pre-marshalled C-ABI arguments of one step (the timed loop then only
+    crosses ctypes once per step)."""
+    from gated_group_rmsnorm_gb300 import binding
+    width = wl.width
+    rows, ys = binding._as_rows(inp.y, width, "y")
+    _, gts = binding._as_rows(inp.gate, width, "gate")
+    _, os_ = binding._as_rows(out, width, "out")
+    return (inp.y.data_ptr(), inp.gate.data_ptr(), inp.w.data_ptr(), out.data_ptr(), rows, width,
+            wl.group_size, ys, gts, os_, ctypes.c_float(wl.eps), binding.DTYPE_CODE[wl.dtype],
+            wl.mode, stream_handle)
+
+
+def _decode_numbers(g, device) -> dict:
+    """µs per call of the batch-1 decode shape: eager, a 1-call graph, a 21-call
+    graph (one Mamba-2 norm per layer of a 21-layer decode step)."""
+    wl = ggrn_inputs.WORKLOADS["mamba2_decode"]
+    layers = [ggrn_inputs.make_inputs(wl, device=device, seed=100 + i) for i in range(21)]
+    outs = [torch.empty_like(l.y) for l in layers]
+    stream = torch.cuda.current_stream(device)
+    L = g.load()
+    handle = ctypes.c_void_p(stream.cuda_stream)
+    args = [_raw_args(g, l, o, wl, handle) for l, o in zip(layers, outs)]
+    n_calls = 2100
+
+    def timed(fn, n):
+        for _ in range(50):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        return e0.elapsed_time(e1) * 1e3, wall * 1e6
+
+    i = [0]
+
+    def eager():
+        st = L.ggrn_forward(*args[i[0] % 21])
+        i[0] += 1
+        assert st == 0
+    dev_us, wall_us = timed(eager, n_calls)
+    g1 = g.DecodeGraph([dict(y=layers[0].y, gate=layers[0].gate, w=layers[0].w, out=outs[0],
+                             group_size=wl.group_size, eps=wl.eps)])
+    g21 = g.DecodeGraph([dict(y=l.y, gate=l.gate, w=l.w, out=o, group_size=wl.group_size,
+                              eps=wl.eps) for l, o in zip(layers, outs)])
+    g1_dev, g1_wall = timed(lambda: g1.replay(stream), n_calls)
+    g21_dev, g21_wall = timed(lambda: g21.replay(stream), n_calls // 21)
+    g1.close()
+    g21.close()
+    return {"workload": "mamba2_decode (1 x 7680, groups of 960, bf16)",
+            "eager_us_per_call": round(max(dev_us, wall_us) / n_calls, 3),
+            "graph1_us_per_call": round(max(g1_dev, g1_wall) / n_calls, 3),
+            "graph21_us_per_call": round(max(g21_dev, g21_wall) / (21 * (n_calls // 21)), 3),
+            "note": "max(device time, host wall time) per call over back-to-back calls"}
+
+
+def _cpu_baseline(wl, budget_s: float = 10.0) -> dict:
+    """The single-threaded oracle on host cores: sample rows of the workload,
+    repeated until the budget is spent."""
+    import oracle
+    sample_rows = min(wl.rows, 256)
+    swl = wl.with_rows(sample_rows)
+    inp = ggrn_inputs.make_inputs(swl)
+    orc = oracle.default()
+    out = torch.empty((sample_rows, wl.width), dtype=wl.dtype)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.forward(inp.y, inp.gate, inp.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode,
+                    out=out)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    bytes_ = swl.algorithmic_bytes() * reps
+    return {"value": round(bytes_ / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "rows_per_s": round(sample_rows * reps / el, 1),
+            "sample": f"{sample_rows} rows of {wl.name} (same recipe), {reps} passes, {el:.1f} s, "
+                      f"single-threaded C++ oracle"}
+
+
+def _e2e(g, wl, steps: int, device) -> dict:
+    """Public API with pinned host buffers, copies inside the timed region."""
+    host = ggrn_inputs.make_inputs(wl, device=device)
+    if host.packed is not None:
+        packed_h = host.packed.cpu().pin_memory()
+        packed_d = torch.empty_like(host.packed)
+        width = wl.width
+        h2d = [(packed_h, packed_d)]
+        y_d, g_d = packed_d[:, :width], packed_d[:, width:2 * width]
+    else:
+        y_h, g_h = host.y.cpu().pin_memory(), host.gate.cpu().pin_memory()
+        y_d, g_d = torch.empty_like(host.y), torch.empty_like(host.gate)
+        h2d = [(y_h, y_d), (g_h, g_d)]
+    w_d = host.w
+    out_d = torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device)
+    out_h = torch.empty((wl.rows, wl.width), dtype=wl.dtype).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for src, dst in h2d:
+            dst.copy_(src, non_blocking=True)
+        g.forward(y_d, g_d, w_d, group_size=wl.group_size, eps=wl.eps, mode=wl.mode, out=out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h2d_bytes = sum(s.numel() * s.element_size() for s, _ in h2d)
+    d2h_bytes = out_h.numel() * out_h.element_size()
+    return {"value": round(wl.algorithmic_bytes() * steps / (ms / 1e3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def run_ours(args) -> None:
+    rank, world, local_rank = dist_env()
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    import gated_group_rmsnorm_gb300 as g
+    L = g.load(build_if_missing=True)
+
+    wl = ggrn_inputs.WORKLOADS[args.workload]
+    bytes_per_step = wl.algorithmic_bytes()
+    n_sets = max(2, -(-4 * L2_BYTES // bytes_per_step))
+    sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
+    outs = [torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(device)
+    handle = ctypes.c_void_p(stream.cuda_stream)
+    raw = [_raw_args(g, s, o, wl, handle) for s, o in zip(sets, outs)]
+    plan = g.plan(sets[0].y, sets[0].gate, sets[0].w, group_size=wl.group_size, mode=wl.mode,
+                  out=outs[0])
+
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+
+    for i in range(args.warmup):
+        st = L.ggrn_forward(*raw[i % n_sets])
+        if st != 0:
+            raise RuntimeError(f"ggrn_forward: {g.status_string(st)}")
+    torch.cuda.synchronize()
+
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        L.ggrn_forward(*raw[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    max_ms = reduce_max(ms, device)
+    sampler.stop()
+    clocks = sampler.summary(t_start, t_end)
+
+    agg = aggregate(bytes_per_step, wl.rows, args.steps, max_ms, world)
+    peak, peak_src = hbm_peak()
+    kernel_gbs = bytes_per_step / (ms / args.steps / 1e3) / 1e9
+    traffic, traffic_note = recorded_traffic(wl.name)
+
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        extra["cpu_baseline"] = _cpu_baseline(wl, args.cpu_seconds)
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(g, wl, args.e2e_steps, device)
+        e2e_ms = reduce_max(e2e["ms_per_step"], device)
+        e2e["value"] = round(world * bytes_per_step / (e2e_ms / 1e3) / 1e9, 2)
+        e2e["ms_per_step"] = round(e2e_ms, 4)
+    decode = _decode_numbers(g, device) if (rank == 0 and not args.no_decode) else None
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(agg["gbs"], 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "width": wl.width,
+                   "group_size": wl.group_size, "io_dtype": IO_DTYPE[wl.dtype],
+                   "mode": "mamba2" if wl.mode == 0 else "onnx", "eps": wl.eps,
+                   "row_stride": wl.packed_width or wl.width,
+                   "l2": f"inputs rotate over {n_sets} copies "
+                         f"({n_sets * bytes_per_step / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2)",
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)",
+                   "path": plan["path_name"], "block_threads": plan["block_threads"],
+                   "grid_blocks": plan["grid_blocks"]},
+        "rows_per_s": round(agg["rows_per_s"], 1),
+        "pct_of_peak": {"of_measured_copy_peak": round(100 * kernel_gbs / peak, 2),
+                        "of_nominal_8TBs": round(100 * kernel_gbs / NOMINAL_HBM_GBS, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
+                     "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": bytes_per_step,
+                     "traffic_note": traffic_note},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    line.update(extra)
+    if decode is not None:
+        line["decode"] = decode
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle.
+# ---------------------------------------------------------------------------
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = ggrn_inputs.WORKLOADS[args.workload]
+    orc = oracle.default()
+    # Calibrate rows per step so that W + K steps take about `ref_seconds`.
+    cal = wl.with_rows(min(wl.rows, 16))
+    cin = ggrn_inputs.make_inputs(cal)
+    t0 = time.perf_counter()
+    orc.forward(cin.y, cin.gate, cin.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
+    per_row = (time.perf_counter() - t0) / cal.rows
+    total_steps = max(1, args.steps + args.warmup)
+    rows = int(max(1, min(wl.rows, args.ref_seconds / total_steps / max(per_row, 1e-9))))
+    swl = wl.with_rows(rows)
+    inp = ggrn_inputs.make_inputs(swl)
+    out = torch.empty((rows, wl.width), dtype=wl.dtype)
+
+    def step():
+        orc.forward(inp.y, inp.gate, inp.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode,
+                    out=out)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    gbs = swl.algorithmic_bytes() * args.steps / el / 1e9
+    sample = (f"{rows} of {wl.rows} rows of {wl.name} per step (same recipe), single-threaded "
+              f"C++ oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "width": wl.width,
+                   "group_size": wl.group_size, "io_dtype": IO_DTYPE[wl.dtype],
+                   "mode": "mamba2" if wl.mode == 0 else "onnx", "sample_rows_per_step": rows},
+        "rows_per_s": round(rows * args.steps / el, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(ggrn_inputs.WORKLOADS), default="mamba2_prefill")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args(argv)
+    _, world, _ = dist_env()
+    if world != args.gpus and args.gpus != 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) fused gated group-RMSNorm.
+
+The operation ("gated_group_rmsnorm" Mojo module page, math block; and
+"com.microsoft.GatedRMSNorm" README, Description): for every row and every
+contiguous group of ``group_size`` columns,
+
+  mamba2: out = cast(w[col] * cast(y*silu(gate) * rsqrt(mean((y*silu(gate))^2) + eps)))
+  onnx:   out = cast(x * rsqrt(mean(x^2) + eps) * scale[j] * silu(gate))
+
+computed by hand-written CUDA kernels behind a C ABI (``include/ggrn.h``,
+``libggrn.so``).  This package is the thin Python binding.
+"""
+from .binding import (BF16, DTYPE_CODE, F16, F32, MAMBA2, ONNX, PATH_AUTO, PATH_NAMES,
+                      PATH_SCALAR, PATH_STRADDLE, PATH_TEAM, PATH_WIDE, DecodeGraph, GgrnError,
+                      forward, ggrn_forward, ggrn_forward_path, ggrn_plan, library_path, load,
+                      plan, status_string)
+
+__all__ = ["forward", "plan", "DecodeGraph", "GgrnError", "ggrn_forward", "ggrn_forward_path",
+           "ggrn_plan", "load", "library_path", "status_string", "MAMBA2", "ONNX", "F32", "F16",
+           "BF16", "PATH_AUTO", "PATH_TEAM", "PATH_WIDE", "PATH_STRADDLE", "PATH_SCALAR",
+           "PATH_NAMES", "DTYPE_CODE"]

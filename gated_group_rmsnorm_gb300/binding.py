@@ -1,0 +1,271 @@
+"""ctypes binding of ``libggrn.so`` (the C ABI declared in ``include/ggrn.h``).
+
+Argument marshalling only: every step of the operation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if the library is missing or a call fails, an
+exception says so.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+# ggrn_status
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_OVERLAP, ERR_CUDA, ERR_UNSUPPORTED, ERR_ARG = range(9)
+# ggrn_dtype / ggrn_mode / ggrn_path
+F32, F16, BF16 = 0, 1, 2
+MAMBA2, ONNX = 0, 1
+PATH_AUTO, PATH_TEAM, PATH_WIDE, PATH_STRADDLE, PATH_SCALAR = range(5)
+PATH_NAMES = {PATH_AUTO: "auto", PATH_TEAM: "team", PATH_WIDE: "wide",
+              PATH_STRADDLE: "straddle", PATH_SCALAR: "scalar"}
+DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
+
+# The exported symbols, as include/ggrn.h declares them.
+EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
+           "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version")
+
+
+class GgrnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        msg = status_string(status) if _lib is not None else f"status {status}"
+        super().__init__(f"{what}: {msg} (status {status})" if what else f"{msg} (status {status})")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("team_lanes", ctypes.c_int32),
+                ("vec_per_lane", ctypes.c_int32), ("elems_per_vec", ctypes.c_int32),
+                ("grid_blocks", ctypes.c_int64), ("block_threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("items", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["path_name"] = PATH_NAMES.get(self.path, "?")
+        return d
+
+
+class Call(ctypes.Structure):
+    _fields_ = [("y", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("rows", ctypes.c_int64), ("width", ctypes.c_int64),
+                ("group_size", ctypes.c_int64), ("y_row_stride", ctypes.c_int64),
+                ("gate_row_stride", ctypes.c_int64), ("out_row_stride", ctypes.c_int64),
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("mode", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load ``libggrn.so`` (building it first if it is missing and allowed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"{path} is not built; run gated_group_rmsnorm_gb300.build")
+            _build.build()
+        L = ctypes.CDLL(path)
+        i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
+        L.ggrn_forward.restype = ci
+        L.ggrn_forward_path.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci,
+                                        ci, vp]
+        L.ggrn_forward_path.restype = ci
+        L.ggrn_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, ci, ci,
+                                ctypes.POINTER(PlanInfo)]
+        L.ggrn_plan.restype = ci
+        L.ggrn_graph_create.argtypes = [ctypes.POINTER(Call), ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_void_p)]
+        L.ggrn_graph_create.restype = ci
+        L.ggrn_graph_launch.argtypes = [vp, vp]
+        L.ggrn_graph_launch.restype = ci
+        L.ggrn_graph_destroy.argtypes = [vp]
+        L.ggrn_graph_destroy.restype = ci
+        L.ggrn_status_string.argtypes = [ci]
+        L.ggrn_status_string.restype = ctypes.c_char_p
+        L.ggrn_version.argtypes = []
+        L.ggrn_version.restype = ci
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return load().ggrn_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# Raw C-ABI calls (same names as the C functions).
+# ---------------------------------------------------------------------------
+def ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride, gate_row_stride,
+                 out_row_stride, eps, dtype, mode, stream) -> int:
+    return load().ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride,
+                               gate_row_stride, out_row_stride, eps, dtype, mode, stream)
+
+
+def ggrn_forward_path(y, gate, w, out, rows, width, group_size, y_row_stride, gate_row_stride,
+                      out_row_stride, eps, dtype, mode, path, stream) -> int:
+    return load().ggrn_forward_path(y, gate, w, out, rows, width, group_size, y_row_stride,
+                                    gate_row_stride, out_row_stride, eps, dtype, mode, path,
+                                    stream)
+
+
+def ggrn_plan(y, gate, w, out, rows, width, group_size, y_row_stride, gate_row_stride,
+              out_row_stride, dtype, mode, path=PATH_AUTO):
+    info = PlanInfo()
+    st = load().ggrn_plan(y, gate, w, out, rows, width, group_size, y_row_stride,
+                          gate_row_stride, out_row_stride, dtype, mode, path, ctypes.byref(info))
+    return st, info
+
+
+# ---------------------------------------------------------------------------
+# Tensor-level API.
+# ---------------------------------------------------------------------------
+def _as_rows(t: torch.Tensor, width: int, name: str) -> tuple[int, int]:
+    """(rows, row_stride) of a tensor viewed as [rows, width] with unit inner stride."""
+    if t.dim() == 0:
+        raise ValueError(f"{name} must have rank >= 1")
+    if t.shape[-1] != width:
+        raise ValueError(f"{name}: last dimension {t.shape[-1]} != width {width}")
+    if t.numel() == 0:
+        return 0, width
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} needs unit stride on its last dimension")
+    if t.dim() == 1:
+        return 1, width
+    lead = t.shape[:-1]
+    rows = 1
+    for s in lead:
+        rows *= s
+    # leading axes must fold into one uniformly strided row axis
+    stride = t.stride(-2)
+    expect = stride
+    for d in range(t.dim() - 2, -1, -1):
+        if t.shape[d] != 1 and t.stride(d) != expect:
+            raise ValueError(f"{name}: leading axes do not fold into one row axis")
+        expect *= t.shape[d]
+    return rows, (stride if rows > 1 else width)
+
+
+def _stream_handle(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def plan(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size: int,
+         mode="mamba2", out: torch.Tensor | None = None, path: int = PATH_AUTO) -> dict:
+    """The launch ``forward`` would make (host only)."""
+    width = y.shape[-1]
+    rows, ys = _as_rows(y, width, "y")
+    _, gts = _as_rows(gate, width, "gate")
+    os_ = width
+    optr = 0
+    if out is not None:
+        _, os_ = _as_rows(out, width, "out")
+        optr = out.data_ptr()
+    st, info = ggrn_plan(y.data_ptr(), gate.data_ptr(), w.data_ptr(), optr, rows, width,
+                         group_size, ys, gts, os_, DTYPE_CODE[y.dtype], MODE_CODE[mode], path)
+    if st != OK:
+        raise GgrnError(st, "ggrn_plan")
+    return info.as_dict()
+
+
+def forward(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size: int,
+            eps: float, mode="mamba2", out: torch.Tensor | None = None,
+            path: int = PATH_AUTO) -> torch.Tensor:
+    """Fused gated group-RMSNorm on CUDA tensors, enqueued on the current stream.
+
+    ``y``, ``gate``: [..., width] tensors of T (f32, f16, bf16; ONNX: f32, f16)
+    whose leading axes fold into rows (row-strided views allowed).
+    ``w``: MAMBA2 -> f32 [width]; ONNX -> T scale with ``group_size`` elements
+    (any of the shapes (C), (1, C), (C, 1)).
+    ``out``: optional output (same shape as y; allocated like y when omitted).
+    """
+    if not y.is_cuda:
+        raise ValueError("forward runs on CUDA tensors only (no CPU path)")
+    m = MODE_CODE[mode]
+    width = y.shape[-1]
+    if gate.shape != y.shape:
+        raise ValueError("gate must have the shape of y")
+    if gate.dtype != y.dtype:
+        raise ValueError("gate must have the dtype of y")
+    if m == MAMBA2 and (w.dtype != torch.float32 or w.numel() != width):
+        raise ValueError("MAMBA2 weight is float32 with `width` elements")
+    if m == ONNX:
+        if w.dtype != y.dtype or w.numel() != group_size:
+            raise ValueError("ONNX scale has the dtype of X and group_size elements")
+        w = w.reshape(-1)
+    if not w.is_contiguous():
+        w = w.contiguous()
+    if out is None:
+        out = torch.empty(y.shape, dtype=y.dtype, device=y.device)
+    elif out.shape != y.shape or out.dtype != y.dtype:
+        raise ValueError("out must have the shape and dtype of y")
+    rows, ys = _as_rows(y, width, "y")
+    _, gts = _as_rows(gate, width, "gate")
+    _, os_ = _as_rows(out, width, "out")
+    if y.dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {y.dtype}")
+    st = ggrn_forward_path(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows,
+                           width, group_size, ys, gts, os_, float(eps), DTYPE_CODE[y.dtype], m,
+                           path, _stream_handle(y.device))
+    if st != OK:
+        raise GgrnError(st, "ggrn_forward")
+    return out
+
+
+class DecodeGraph:
+    """A chain of calls captured once into a CUDA graph and replayed with one launch.
+
+    ``calls``: list of dicts with the tensors and arguments of ``forward``
+    (``y``, ``gate``, ``w``, ``out``, ``group_size``, ``eps``, ``mode``).  The
+    tensors are baked into the graph: keep them alive and refill them in
+    place between replays.
+    """
+
+    def __init__(self, calls: list[dict]):
+        arr = (Call * len(calls))()
+        self._keep = []
+        for i, c in enumerate(calls):
+            y, gate, w, out = c["y"], c["gate"], c["w"], c["out"]
+            width = y.shape[-1]
+            rows, ys = _as_rows(y, width, "y")
+            _, gts = _as_rows(gate, width, "gate")
+            _, os_ = _as_rows(out, width, "out")
+            arr[i] = Call(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows, width,
+                          c["group_size"], ys, gts, os_, float(c["eps"]), DTYPE_CODE[y.dtype],
+                          MODE_CODE[c.get("mode", "mamba2")])
+            self._keep.extend([y, gate, w, out])
+        self._handle = ctypes.c_void_p()
+        st = load().ggrn_graph_create(arr, len(calls), ctypes.byref(self._handle))
+        if st != OK:
+            raise GgrnError(st, "ggrn_graph_create")
+        self.device = calls[0]["y"].device
+
+    def replay(self, stream: torch.cuda.Stream | None = None) -> None:
+        s = stream.cuda_stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        st = load().ggrn_graph_launch(self._handle, ctypes.c_void_p(s))
+        if st != OK:
+            raise GgrnError(st, "ggrn_graph_launch")
+
+    def close(self) -> None:
+        if self._handle:
+            load().ggrn_graph_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

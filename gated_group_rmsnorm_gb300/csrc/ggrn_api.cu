@@ -1,0 +1,457 @@
+// ggrn_api.cu -- the C ABI declared in include/ggrn.h: argument validation,
+// kernel-family selection, launch, decode graphs and status strings.
+//
+// Selection follows the shape and the layout, the way the ONNX-contrib
+// README's implementation variants are picked per call from device
+// capabilities, shapes and dtypes ("com.microsoft.GatedRMSNorm" README,
+// Implementation variants); here every family runs on every sm_103a device,
+// so only the shape and the alignment decide.  A group size that is not a
+// multiple of the warp or of the vector width needs no special contract
+// ("gated_group_rmsnorm" Mojo module page, Parallelization).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ggrn.h"
+#include "ggrn_internal.h"
+
+namespace ggrn {
+namespace {
+
+constexpr int kDefaultSMs = 152;
+constexpr int kTeamBlock = 256;
+constexpr int kTeamMaxVec = 128;     // TEAM covers groups of up to 128 vectors
+constexpr int kWideVpl = 4;
+constexpr int kWideMaxThreads = 1024;
+constexpr int kStraddleVpl = 4;
+constexpr int kStraddleMaxThreads = 256;
+constexpr int kScalarBlock = 256;
+constexpr int64_t kMaxGrid = 0x7fffffff;
+
+int elem_size(int dtype) { return dtype == kF32 ? 4 : 2; }
+
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();  // clear the "no device" error this query may set
+    return kDefaultSMs;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = kDefaultSMs;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t gcd64(int64_t a, int64_t b) {
+  while (b) {
+    int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// Byte extent of a [rows, width] matrix with row stride `stride` elements;
+// false when it does not fit in int64.
+bool extent_bytes(int64_t rows, int64_t width, int64_t stride, int es, int64_t* out) {
+  if (rows == 0) {
+    *out = 0;
+    return true;
+  }
+  __int128 n = static_cast<__int128>(rows - 1) * stride + width;
+  n *= es;
+  if (n > static_cast<__int128>(INT64_MAX)) return false;
+  *out = static_cast<int64_t>(n);
+  return true;
+}
+
+bool ranges_overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (na == 0 || nb == 0) return false;
+  uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
+}
+
+// Checks shared by every entry point (pointers are only checked when rows > 0).
+// `out_optional`: ggrn_plan accepts out == NULL (an output not allocated yet).
+int validate(const Args& a, bool out_optional = false) {
+  if (a.dtype != kF32 && a.dtype != kF16 && a.dtype != kBF16) return GGRN_ERR_DTYPE;
+  if (a.mode != kMamba2 && a.mode != kOnnx) return GGRN_ERR_DTYPE;
+  if (a.mode == kOnnx && a.dtype == kBF16) return GGRN_ERR_DTYPE;
+  if (a.rows < 0 || a.width <= 0 || a.gs <= 0 || a.width % a.gs != 0) return GGRN_ERR_SHAPE;
+  if (a.rows > 1 && (a.ys < a.width || a.gts < a.width || a.os < a.width)) return GGRN_ERR_SHAPE;
+  if (a.rows == 0) return GGRN_OK;
+  const int es = elem_size(a.dtype);
+  int64_t ny, ng, no;
+  const int64_t ys = a.rows > 1 ? a.ys : a.width, gts = a.rows > 1 ? a.gts : a.width,
+                os = a.rows > 1 ? a.os : a.width;
+  if (!extent_bytes(a.rows, a.width, ys, es, &ny) || !extent_bytes(a.rows, a.width, gts, es, &ng) ||
+      !extent_bytes(a.rows, a.width, os, es, &no))
+    return GGRN_ERR_SHAPE;
+  if (a.rows > INT64_MAX / (a.width / a.gs)) return GGRN_ERR_SHAPE;
+  if (!a.y || !a.gate || !a.w || (!a.out && !out_optional)) return GGRN_ERR_NULL;
+  const int wes = a.mode == kMamba2 ? 4 : es;
+  if (!aligned(a.y, es) || !aligned(a.gate, es) || !aligned(a.out, es) || !aligned(a.w, wes))
+    return GGRN_ERR_ALIGN;
+  if (!a.out) return GGRN_OK;
+  const int64_t nw = (a.mode == kMamba2 ? a.width : a.gs) * wes;
+  if (ranges_overlap(a.out, no, a.y, ny) || ranges_overlap(a.out, no, a.gate, ng) ||
+      ranges_overlap(a.out, no, a.w, nw))
+    return GGRN_ERR_OVERLAP;
+  return GGRN_OK;
+}
+
+// May the 16-byte vector families load this call's buffers?
+bool vector_layout_ok(const Args& a) {
+  const int es = elem_size(a.dtype);
+  if (!aligned(a.y, 16) || !aligned(a.gate, 16) || !aligned(a.out, 16) || !aligned(a.w, 16))
+    return false;
+  if (a.rows > 1 &&
+      ((a.ys * es) % 16 != 0 || (a.gts * es) % 16 != 0 || (a.os * es) % 16 != 0))
+    return false;
+  return true;
+}
+
+int next_pow2(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// One item per team or CTA; grid capped at the launch limit (the kernels
+// stride over the remaining items).
+int plan_team(const Args& a, Plan* p) {
+  const int es = elem_size(a.dtype);
+  const int E = 16 / es;
+  if (a.gs % E != 0) return GGRN_ERR_UNSUPPORTED;
+  const int64_t nvec = a.gs / E;
+  if (nvec > kTeamMaxVec) return GGRN_ERR_UNSUPPORTED;
+  p->path = kTeam;
+  p->elems_per_vec = E;
+  p->nvec = static_cast<int>(nvec);
+  if (nvec <= 32) {
+    p->lanes = next_pow2(static_cast<int>(nvec));
+    p->vpl = 1;
+  } else {
+    p->lanes = 32;
+    p->vpl = nvec <= 64 ? 2 : 4;
+  }
+  p->groups = a.width / a.gs;
+  p->items = a.rows * p->groups;
+  // Spread small problems over the SMs: shrink the block (down to one warp)
+  // while that keeps the grid under one CTA per SM.
+  const int sms = sm_count();
+  int block = kTeamBlock;
+  const int64_t per_warp = 32 / p->lanes;
+  while (block > 32 && ceil_div(p->items, (block / 32) * per_warp) < sms) block /= 2;
+  p->block = block;
+  p->grid = std::min<int64_t>(kMaxGrid, std::max<int64_t>(1, ceil_div(p->items, (block / 32) * per_warp)));
+  if (p->items == 0) p->grid = 0;
+  p->smem = 0;
+  return GGRN_OK;
+}
+
+int plan_wide(const Args& a, Plan* p) {
+  const int es = elem_size(a.dtype);
+  const int E = 16 / es;
+  if (a.gs % E != 0) return GGRN_ERR_UNSUPPORTED;
+  const int64_t nvec = a.gs / E;
+  const int64_t threads = ceil_div(ceil_div(nvec, kWideVpl), 32) * 32;
+  if (threads > kWideMaxThreads) return GGRN_ERR_UNSUPPORTED;
+  p->path = kWide;
+  p->elems_per_vec = E;
+  p->nvec = static_cast<int>(nvec);
+  p->lanes = static_cast<int>(threads);
+  p->vpl = kWideVpl;
+  p->block = static_cast<int>(threads);
+  p->groups = a.width / a.gs;
+  p->items = a.rows * p->groups;
+  p->grid = std::min<int64_t>(kMaxGrid, p->items);
+  p->smem = 0;
+  return GGRN_OK;
+}
+
+int plan_straddle(const Args& a, Plan* p) {
+  const int es = elem_size(a.dtype);
+  const int E = 16 / es;
+  if (a.gs % E == 0 || a.gs < E) return GGRN_ERR_UNSUPPORTED;
+  const int64_t lcm = a.gs / gcd64(a.gs, E) * E;     // elements per period
+  const int64_t period_vecs = lcm / E;
+  const int64_t max_vecs = static_cast<int64_t>(kStraddleMaxThreads) * kStraddleVpl;
+  if (period_vecs > max_vecs) return GGRN_ERR_UNSUPPORTED;
+  const int64_t periods_per_row = ceil_div(a.width, lcm);
+  const int64_t m = std::max<int64_t>(1, std::min<int64_t>(periods_per_row, max_vecs / period_vecs));
+  p->path = kStraddle;
+  p->elems_per_vec = E;
+  p->vpl = kStraddleVpl;
+  p->chunk_elems = m * lcm;
+  p->chunks_per_row = ceil_div(a.width, p->chunk_elems);
+  const int64_t nv_max = ceil_div(std::min<int64_t>(p->chunk_elems, a.width), E);
+  p->nvec = static_cast<int>(nv_max);
+  p->chunk_groups = static_cast<int>(std::min<int64_t>(p->chunk_elems, a.width) / a.gs);
+  p->block = static_cast<int>(ceil_div(ceil_div(nv_max, kStraddleVpl), 32) * 32);
+  p->lanes = p->block;
+  p->groups = a.width / a.gs;
+  p->items = a.rows * p->chunks_per_row;
+  p->grid = std::min<int64_t>(kMaxGrid, p->items);
+  p->smem = static_cast<int>((2 * nv_max + p->chunk_groups) * sizeof(float));
+  return GGRN_OK;
+}
+
+int plan_scalar(const Args& a, Plan* p) {
+  p->path = kScalar;
+  p->elems_per_vec = 1;
+  p->vpl = 1;
+  p->lanes = a.gs <= 16 ? 1 : 32;
+  p->groups = a.width / a.gs;
+  p->items = a.rows * p->groups;
+  p->block = kScalarBlock;
+  const int64_t teams_per_block = (kScalarBlock / 32) * (32 / p->lanes);
+  p->grid = std::min<int64_t>(kMaxGrid, ceil_div(p->items, teams_per_block));
+  p->smem = 0;
+  p->nvec = 0;
+  return GGRN_OK;
+}
+
+int make_plan(const Args& a, int path, Plan* p) {
+  *p = Plan();
+  const bool vec_ok = vector_layout_ok(a);
+  switch (path) {
+    case kAuto: {
+      if (vec_ok) {
+        if (plan_team(a, p) == GGRN_OK) return GGRN_OK;
+        if (plan_wide(a, p) == GGRN_OK) return GGRN_OK;
+        if (plan_straddle(a, p) == GGRN_OK) return GGRN_OK;
+      }
+      return plan_scalar(a, p);
+    }
+    case kTeam:
+      if (!vec_ok) return GGRN_ERR_ALIGN;
+      return plan_team(a, p);
+    case kWide:
+      if (!vec_ok) return GGRN_ERR_ALIGN;
+      return plan_wide(a, p);
+    case kStraddle:
+      if (!vec_ok) return GGRN_ERR_ALIGN;
+      return plan_straddle(a, p);
+    case kScalar:
+      return plan_scalar(a, p);
+    default:
+      return GGRN_ERR_ARG;
+  }
+}
+
+Args make_args(const void* y, const void* gate, const void* w, void* out, int64_t rows,
+               int64_t width, int64_t gs, int64_t ys, int64_t gts, int64_t os, float eps,
+               int dtype, int mode) {
+  Args a;
+  a.y = y;
+  a.gate = gate;
+  a.w = w;
+  a.out = out;
+  a.rows = rows;
+  a.width = width;
+  a.gs = gs;
+  // A single row has no row stride to speak of.
+  a.ys = rows > 1 ? ys : width;
+  a.gts = rows > 1 ? gts : width;
+  a.os = rows > 1 ? os : width;
+  a.eps = eps;
+  a.dtype = dtype;
+  a.mode = mode;
+  return a;
+}
+
+int launch(const Args& a, const Plan& p, cudaStream_t s) {
+  if (p.grid == 0) return GGRN_OK;
+  const KParams k = make_params(a, p);
+  cudaError_t e;
+  switch (a.dtype) {
+    case kF32: e = launch_f32(k, p, a.mode, s); break;
+    case kF16: e = launch_f16(k, p, a.mode, s); break;
+    default: e = launch_bf16(k, p, a.mode, s); break;
+  }
+  return e == cudaSuccess ? GGRN_OK : GGRN_ERR_CUDA;
+}
+
+int forward_impl(const Args& a, int path, cudaStream_t s) {
+  int st = validate(a);
+  if (st != GGRN_OK || a.rows == 0) return st;
+  Plan p;
+  st = make_plan(a, path, &p);
+  if (st != GGRN_OK) return st;
+  return launch(a, p, s);
+}
+
+struct DecodeGraph {
+  cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace
+
+KParams make_params(const Args& a, const Plan& p) {
+  KParams k;
+  k.y = a.y;
+  k.gate = a.gate;
+  k.w = a.w;
+  k.out = a.out;
+  k.items = p.items;
+  k.groups = p.groups;
+  k.width = a.width;
+  k.gs = a.gs;
+  k.ys = a.ys;
+  k.gts = a.gts;
+  k.os = a.os;
+  k.chunk_elems = p.chunk_elems;
+  k.chunks_per_row = p.chunks_per_row;
+  k.nvec = p.nvec;
+  k.chunk_groups = p.chunk_groups;
+  k.eps = a.eps;
+  k.gs_f = static_cast<float>(a.gs);
+  return k;
+}
+
+}  // namespace ggrn
+
+using namespace ggrn;
+
+extern "C" int ggrn_forward(const void* y, const void* gate, const void* w, void* out,
+                            int64_t rows, int64_t width, int64_t group_size,
+                            int64_t y_row_stride, int64_t gate_row_stride,
+                            int64_t out_row_stride, float eps, int dtype, int mode,
+                            void* cuda_stream) {
+  const Args a = make_args(y, gate, w, out, rows, width, group_size, y_row_stride,
+                           gate_row_stride, out_row_stride, eps, dtype, mode);
+  return forward_impl(a, kAuto, static_cast<cudaStream_t>(cuda_stream));
+}
+
+extern "C" int ggrn_forward_path(const void* y, const void* gate, const void* w, void* out,
+                                 int64_t rows, int64_t width, int64_t group_size,
+                                 int64_t y_row_stride, int64_t gate_row_stride,
+                                 int64_t out_row_stride, float eps, int dtype, int mode,
+                                 int path, void* cuda_stream) {
+  if (path < kAuto || path > kScalar) return GGRN_ERR_ARG;
+  const Args a = make_args(y, gate, w, out, rows, width, group_size, y_row_stride,
+                           gate_row_stride, out_row_stride, eps, dtype, mode);
+  return forward_impl(a, path, static_cast<cudaStream_t>(cuda_stream));
+}
+
+extern "C" int ggrn_plan(const void* y, const void* gate, const void* w, const void* out,
+                         int64_t rows, int64_t width, int64_t group_size, int64_t y_row_stride,
+                         int64_t gate_row_stride, int64_t out_row_stride, int dtype, int mode,
+                         int path, ggrn_plan_info* info) {
+  if (!info) return GGRN_ERR_ARG;
+  if (path < kAuto || path > kScalar) return GGRN_ERR_ARG;
+  std::memset(info, 0, sizeof(*info));
+  const Args a = make_args(y, gate, w, const_cast<void*>(out), rows, width, group_size,
+                           y_row_stride, gate_row_stride, out_row_stride, 0.0f, dtype, mode);
+  int st = validate(a, /*out_optional=*/true);
+  if (st != GGRN_OK) return st;
+  Plan p;
+  st = make_plan(a, path, &p);
+  if (st != GGRN_OK) return st;
+  info->path = p.path;
+  info->team_lanes = p.lanes;
+  info->vec_per_lane = p.vpl;
+  info->elems_per_vec = p.elems_per_vec;
+  info->grid_blocks = p.grid;
+  info->block_threads = p.block;
+  info->smem_bytes = p.smem;
+  info->items = p.items;
+  return GGRN_OK;
+}
+
+extern "C" int ggrn_graph_create(const ggrn_call* calls, int32_t n, void** graph) {
+  if (!graph || n <= 0 || !calls) return GGRN_ERR_ARG;
+  *graph = nullptr;
+  // Validate and plan every call before capturing anything.
+  for (int32_t i = 0; i < n; ++i) {
+    const ggrn_call& c = calls[i];
+    const Args a = make_args(c.y, c.gate, c.w, c.out, c.rows, c.width, c.group_size,
+                             c.y_row_stride, c.gate_row_stride, c.out_row_stride, c.eps, c.dtype,
+                             c.mode);
+    int st = validate(a);
+    if (st != GGRN_OK) return st;
+    Plan p;
+    if (a.rows > 0 && (st = make_plan(a, kAuto, &p)) != GGRN_OK) return st;
+  }
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GGRN_ERR_CUDA;
+  int status = GGRN_OK;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return GGRN_ERR_CUDA;
+  }
+  for (int32_t i = 0; i < n && status == GGRN_OK; ++i) {
+    const ggrn_call& c = calls[i];
+    const Args a = make_args(c.y, c.gate, c.w, c.out, c.rows, c.width, c.group_size,
+                             c.y_row_stride, c.gate_row_stride, c.out_row_stride, c.eps, c.dtype,
+                             c.mode);
+    status = forward_impl(a, kAuto, s);
+  }
+  cudaError_t e = cudaStreamEndCapture(s, &g);
+  if (status == GGRN_OK && e != cudaSuccess) status = GGRN_ERR_CUDA;
+  DecodeGraph* dg = nullptr;
+  if (status == GGRN_OK) {
+    dg = new DecodeGraph();
+    if (cudaGraphInstantiate(&dg->exec, g, 0) != cudaSuccess) {
+      status = GGRN_ERR_CUDA;
+      delete dg;
+      dg = nullptr;
+    }
+  }
+  if (g) cudaGraphDestroy(g);
+  cudaStreamDestroy(s);
+  if (status == GGRN_OK) *graph = dg;
+  return status;
+}
+
+extern "C" int ggrn_graph_launch(void* graph, void* cuda_stream) {
+  if (!graph) return GGRN_ERR_ARG;
+  DecodeGraph* dg = static_cast<DecodeGraph*>(graph);
+  return cudaGraphLaunch(dg->exec, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+             ? GGRN_OK
+             : GGRN_ERR_CUDA;
+}
+
+extern "C" int ggrn_graph_destroy(void* graph) {
+  if (!graph) return GGRN_OK;
+  DecodeGraph* dg = static_cast<DecodeGraph*>(graph);
+  cudaError_t e = cudaGraphExecDestroy(dg->exec);
+  delete dg;
+  return e == cudaSuccess ? GGRN_OK : GGRN_ERR_CUDA;
+}
+
+extern "C" const char* ggrn_status_string(int status) {
+  switch (status) {
+    case GGRN_OK: return "ok";
+    case GGRN_ERR_NULL: return "a required pointer is NULL";
+    case GGRN_ERR_SHAPE: return "invalid shape: rows < 0, width <= 0, group_size <= 0, width not a "
+                                "multiple of group_size, row stride < width, or size overflow";
+    case GGRN_ERR_ALIGN: return "pointers or row strides not aligned for the requested path";
+    case GGRN_ERR_DTYPE: return "unsupported dtype/mode (ONNX semantics admit float32 and float16)";
+    case GGRN_ERR_OVERLAP: return "out overlaps y, gate or w";
+    case GGRN_ERR_CUDA: return "CUDA runtime error";
+    case GGRN_ERR_UNSUPPORTED: return "the requested path does not cover this shape";
+    case GGRN_ERR_ARG: return "invalid argument (path id, NULL out-parameter or call list)";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int ggrn_version(void) { return 100; }

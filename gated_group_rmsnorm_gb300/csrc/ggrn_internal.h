@@ -1,0 +1,72 @@
+// ggrn_internal.h -- host-side plan and launch interface shared by the C ABI
+// (ggrn_api.cu) and the per-dtype kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ggrn {
+
+enum Mode : int { kMamba2 = 0, kOnnx = 1 };
+enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Path : int { kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4 };
+
+// Validated arguments of one call.
+struct Args {
+  const void* y;
+  const void* gate;
+  const void* w;
+  void* out;
+  int64_t rows, width, gs;
+  int64_t ys, gts, os;  // row strides, elements
+  float eps;
+  int dtype, mode;
+};
+
+// A launch decision.
+struct Plan {
+  int path = kAuto;
+  int lanes = 0;        // TEAM: lanes per group (1..32)
+  int vpl = 0;          // 16-byte vectors per lane per tensor
+  int elems_per_vec = 1;
+  int block = 0;        // threads per CTA
+  int smem = 0;         // dynamic shared memory bytes
+  int64_t grid = 0;     // CTAs
+  int64_t items = 0;    // groups, or row chunks (STRADDLE)
+  int64_t groups = 0;   // groups per row
+  int nvec = 0;         // TEAM/WIDE: vectors per group; STRADDLE: vectors per chunk (max)
+  // STRADDLE
+  int64_t chunk_elems = 0;     // elements per chunk (a multiple of lcm(gs, E))
+  int64_t chunks_per_row = 0;
+  int chunk_groups = 0;        // groups per full chunk
+};
+
+// Kernel parameters (passed by value).
+struct KParams {
+  const void* y;
+  const void* gate;
+  const void* w;
+  void* out;
+  int64_t items;
+  int64_t groups;          // groups per row
+  int64_t width;
+  int64_t gs;
+  int64_t ys, gts, os;
+  int64_t chunk_elems;
+  int64_t chunks_per_row;
+  int nvec;
+  int chunk_groups;
+  float eps;
+  float gs_f;
+};
+
+KParams make_params(const Args& a, const Plan& p);
+
+// Launchers, one per element type (defined in ggrn_kernels_<T>.cu).  They
+// enqueue the kernel the plan names with programmatic dependent launch
+// allowed, and return the CUDA error of the launch.
+cudaError_t launch_f32(const KParams& k, const Plan& p, int mode, cudaStream_t s);
+cudaError_t launch_f16(const KParams& k, const Plan& p, int mode, cudaStream_t s);
+cudaError_t launch_bf16(const KParams& k, const Plan& p, int mode, cudaStream_t s);
+
+}  // namespace ggrn

@@ -1,0 +1,647 @@
+// ggrn_kernels.cuh -- sm_103a kernels of the fused gated group-RMSNorm.
+//
+// The operation ("gated_group_rmsnorm" Mojo module page, math block; and
+// "com.microsoft.GatedRMSNorm" README, Description), per row and per group of
+// gs contiguous columns:
+//   MAMBA2: gated = y*silu(gate); m2 = sum gated^2; nf = rsqrt(m2/gs + eps);
+//           out = cast_T(w[col] * cast_T(gated*nf))
+//   ONNX:   m2 = sum x^2; nf as above; out = cast_T(((x*nf)*scale[j])*silu(gate))
+//
+// The op is a streaming reduction bound by HBM bandwidth: each element of y
+// and gate is read once and each output written once (6 bytes per element for
+// 16-bit T).  Every family below keeps the whole group on chip between the
+// reduction and the epilogue so nothing is re-read from HBM, moves data in
+// 16-byte vectors (8 x 16-bit or 4 x f32 per lane per instruction, one
+// contiguous 512-byte run per warp instruction when a warp covers a group),
+// marks y/gate loads L1::no_allocate and output stores evict-first so the
+// small weight stays cached, and reduces in f32 with warp shuffles.
+//
+// Families:
+//   k_team      a team of LANES (1..32, power of two) lanes of one warp per
+//               group, VPL vectors per lane; a segmented xor butterfly over the
+//               low lane bits reduces each team independently, so 32/LANES
+//               groups share a warp with no shared memory and no barrier.
+//   k_wide      one CTA per group; warp butterflies, then one shared-memory
+//               exchange and one barrier.
+//   k_straddle  one CTA per row chunk holding whole groups, for group sizes
+//               that are not a multiple of the vector: each vector's squares
+//               are split at the (at most one) group boundary it crosses, the
+//               two partials go to shared memory, and one thread per group
+//               adds its vectors' partials in a fixed order.
+//   k_scalar    element loads, LANES lanes per group, two passes over the
+//               group (a correctness path for any alignment and size).
+//
+// All reductions have a fixed order, so results are deterministic.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ggrn_internal.h"
+
+namespace ggrn {
+
+// ---------------------------------------------------------------------------
+// Element traits: 16-byte vector width, unpack/pack, rounding to T.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int E = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[E]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[E]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ __forceinline__ static void round_pair(float& a, float& b) { (void)a, (void)b; }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __ldg(static_cast<const float*>(p) + i);
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    static_cast<float*>(p)[i] = v;
+  }
+  // Accurate exp for f32 outputs (their tolerance is relative, 1e-5).
+  __device__ __forceinline__ static float exp_neg(float x) { return expf(-x); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static void unpack2(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // RNE
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[E]) {
+    unpack2(v.x, f[0], f[1]);
+    unpack2(v.y, f[2], f[3]);
+    unpack2(v.z, f[4], f[5]);
+    unpack2(v.w, f[6], f[7]);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[E]) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+  __device__ __forceinline__ static void round_pair(float& a, float& b) { unpack2(pack2(a, b), a, b); }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    unsigned short h = __ldg(static_cast<const unsigned short*>(p) + i);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+  __device__ __forceinline__ static float exp_neg(float x) { return __expf(-x); }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static void unpack2(uint32_t u, float& lo, float& hi) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);  // RNE
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[E]) {
+    unpack2(v.x, f[0], f[1]);
+    unpack2(v.y, f[2], f[3]);
+    unpack2(v.z, f[4], f[5]);
+    unpack2(v.w, f[6], f[7]);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[E]) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+  __device__ __forceinline__ static void round_pair(float& a, float& b) { unpack2(pack2(a, b), a, b); }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __half2float(__ldg(static_cast<const __half*>(p) + i));
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    static_cast<__half*>(p)[i] = __float2half_rn(v);
+  }
+  __device__ __forceinline__ static float exp_neg(float x) { return __expf(-x); }
+};
+
+// ---------------------------------------------------------------------------
+// Memory helpers.
+// ---------------------------------------------------------------------------
+// 16-byte streaming load: read-only path, no L1 allocation (y and gate are
+// read exactly once).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// 16-byte evict-first store (out is written once and not re-read here).
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+  __stcs(static_cast<uint4*>(p), v);
+}
+
+// 16-byte cached load of the weight (re-read by every row; stays in L1/L2).
+__device__ __forceinline__ uint4 ld_weight(const void* p) {
+  return __ldg(static_cast<const uint4*>(p));
+}
+
+// Programmatic dependent launch: wait for the previous kernel in the stream
+// (its writes visible) before touching global memory; let the next kernel's
+// CTAs be scheduled as soon as ours have all started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Math helpers.
+// ---------------------------------------------------------------------------
+// silu(b) = b / (1 + exp(-b)), f32.  The fast divide returns 0 for
+// denominators above 2^126; there the quotient is still a normal float, so
+// that (rare) case takes the IEEE divide.
+template <typename T>
+__device__ __forceinline__ float silu(float b) {
+  const float d = 1.0f + Elem<T>::exp_neg(b);
+  float s = __fdividef(b, d);
+  if (d > 0x1p126f) s = b / d;
+  return s;
+}
+
+// nf = rsqrt(m2 / gs + eps): IEEE divide, then a correctly rounded rsqrt
+// (once per group, so the exact forms cost nothing).
+__device__ __forceinline__ float normaliser(float m2, float gs_f, float eps) {
+  return __frsqrt_rn(__fdiv_rn(m2, gs_f) + eps);
+}
+
+// Mamba-2 epilogue on one vector: out = cast_T(w * cast_T(gated * nf)).
+template <typename T>
+__device__ __forceinline__ uint4 epilogue_mamba2(const float (&gated)[Elem<T>::E], float nf,
+                                                 const float* wv) {
+  constexpr int E = Elem<T>::E;
+  float t[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) t[e] = gated[e] * nf;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) Elem<T>::round_pair(t[e], t[e + 1]);
+#pragma unroll
+  for (int e = 0; e < E; ++e) t[e] = wv[e] * t[e];
+  return Elem<T>::pack(t);
+}
+
+// ONNX epilogue on one vector: out = cast_T(((x * nf) * scale) * silu(gate)).
+template <typename T>
+__device__ __forceinline__ uint4 epilogue_onnx(const float (&x)[Elem<T>::E],
+                                               const float (&sg)[Elem<T>::E], float nf,
+                                               const float (&sc)[Elem<T>::E]) {
+  constexpr int E = Elem<T>::E;
+  float r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) r[e] = ((x[e] * nf) * sc[e]) * sg[e];
+  return Elem<T>::pack(r);
+}
+
+// Weight of one vector: MAMBA2 -> E floats of w at column col (16-byte
+// aligned); ONNX -> E values of scale (T) at index j, widened.
+template <typename T, int MODE>
+__device__ __forceinline__ void load_weight_vec(const void* w, int64_t idx, float (&wv)[Elem<T>::E]) {
+  constexpr int E = Elem<T>::E;
+  if (MODE == kMamba2) {
+    const float* wp = static_cast<const float*>(w) + idx;
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      uint4 u = ld_weight(wp + 4 * q);
+      wv[4 * q + 0] = __uint_as_float(u.x);
+      wv[4 * q + 1] = __uint_as_float(u.y);
+      wv[4 * q + 2] = __uint_as_float(u.z);
+      wv[4 * q + 3] = __uint_as_float(u.w);
+    }
+  } else {
+    uint4 u = ld_weight(static_cast<const T*>(w) + idx);
+    Elem<T>::unpack(u, wv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TEAM: LANES lanes per group, VPL 16-byte vectors per lane per tensor.
+// Vector v of a group (0 <= v < nvec) sits in slot k = v / LANES of lane
+// v % LANES, so each load instruction of a team covers LANES consecutive
+// vectors.  Teams are aligned LANES-lane segments of a warp; the xor
+// butterfly with offsets < LANES never crosses a segment.
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int LANES, int VPL>
+__global__ void __launch_bounds__(256) k_team(const KParams p) {
+  constexpr int E = Elem<T>::E;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int lane = threadIdx.x & (LANES - 1);
+  const int teams_per_warp = 32 / LANES;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int team_in_warp = (threadIdx.x & 31) / LANES;
+
+  for (int64_t base = warp_id * teams_per_warp; base < p.items;
+       base += warps_total * teams_per_warp) {
+    const int64_t item = base + team_in_warp;
+    const bool active = item < p.items;
+    int64_t row = 0, g = 0;
+    if (active) {
+      row = item / p.groups;
+      g = item - row * p.groups;
+    }
+    const int64_t col0 = g * p.gs;
+    const T* yp = static_cast<const T*>(p.y) + row * p.ys + col0;
+    const T* gp = static_cast<const T*>(p.gate) + row * p.gts + col0;
+
+    uint4 yr[VPL], gr[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * LANES + lane;
+      if (active && v < p.nvec) {
+        yr[k] = ld_stream(yp + (int64_t)v * E);
+        gr[k] = ld_stream(gp + (int64_t)v * E);
+      } else {
+        yr[k] = make_uint4(0u, 0u, 0u, 0u);
+        gr[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+
+    float a[VPL][E];   // MAMBA2: gated; ONNX: x
+    float sg[MODE == kOnnx ? VPL : 1][E];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      float yf[E], gf[E];
+      Elem<T>::unpack(yr[k], yf);
+      Elem<T>::unpack(gr[k], gf);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (MODE == kMamba2) {
+          a[k][e] = yf[e] * silu<T>(gf[e]);
+        } else {
+          a[k][e] = yf[e];
+          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
+        }
+        ss = fmaf(a[k][e], a[k][e], ss);
+      }
+    }
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float nf = normaliser(ss, p.gs_f, p.eps);
+
+    T* op = static_cast<T*>(p.out) + row * p.os + col0;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * LANES + lane;
+      if (active && v < p.nvec) {
+        float wv[E];
+        uint4 o;
+        if (MODE == kMamba2) {
+          load_weight_vec<T, MODE>(p.w, col0 + (int64_t)v * E, wv);
+          o = epilogue_mamba2<T>(a[k], nf, wv);
+        } else {
+          load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
+          o = epilogue_onnx<T>(a[k], sg[MODE == kOnnx ? k : 0], nf, wv);
+        }
+        st_stream(op + (int64_t)v * E, o);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// WIDE: one CTA per group, VPL vectors per thread; vector v sits in slot
+// v / blockDim of thread v % blockDim.  Warp partials meet in shared memory
+// (double-buffered by loop parity, so one barrier per group suffices) and
+// every thread adds them in the same order.
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int VPL, int MAXT>
+__global__ void __launch_bounds__(MAXT) k_wide(const KParams p) {
+  constexpr int E = Elem<T>::E;
+  __shared__ float red[2][32];
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  const int nwarps = nthreads >> 5;
+  int parity = 0;
+  for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x, parity ^= 1) {
+    const int64_t row = item / p.groups;
+    const int64_t g = item - row * p.groups;
+    const int64_t col0 = g * p.gs;
+    const T* yp = static_cast<const T*>(p.y) + row * p.ys + col0;
+    const T* gp = static_cast<const T*>(p.gate) + row * p.gts + col0;
+
+    uint4 yr[VPL], gr[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * nthreads + tid;
+      if (v < p.nvec) {
+        yr[k] = ld_stream(yp + (int64_t)v * E);
+        gr[k] = ld_stream(gp + (int64_t)v * E);
+      } else {
+        yr[k] = make_uint4(0u, 0u, 0u, 0u);
+        gr[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float a[VPL][E];
+    float sg[MODE == kOnnx ? VPL : 1][E];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      float yf[E], gf[E];
+      Elem<T>::unpack(yr[k], yf);
+      Elem<T>::unpack(gr[k], gf);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (MODE == kMamba2) {
+          a[k][e] = yf[e] * silu<T>(gf[e]);
+        } else {
+          a[k][e] = yf[e];
+          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
+        }
+        ss = fmaf(a[k][e], a[k][e], ss);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
+    __syncthreads();
+    float m2 = 0.0f;
+    for (int i = 0; i < nwarps; ++i) m2 += red[parity][i];
+    const float nf = normaliser(m2, p.gs_f, p.eps);
+
+    T* op = static_cast<T*>(p.out) + row * p.os + col0;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * nthreads + tid;
+      if (v < p.nvec) {
+        float wv[E];
+        uint4 o;
+        if (MODE == kMamba2) {
+          load_weight_vec<T, MODE>(p.w, col0 + (int64_t)v * E, wv);
+          o = epilogue_mamba2<T>(a[k], nf, wv);
+        } else {
+          load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
+          o = epilogue_onnx<T>(a[k], sg[MODE == kOnnx ? k : 0], nf, wv);
+        }
+        st_stream(op + (int64_t)v * E, o);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// STRADDLE: group size not a multiple of E (and larger than E).  One CTA per
+// chunk of a row: chunks start at multiples of lcm(gs, E) elements, so they
+// start 16-byte aligned and hold whole groups.  A vector then touches at most
+// two groups; its squares are split at the boundary into (lo, hi) partials.
+// Shared memory: part_lo[nvec], part_hi[nvec], nf[chunk_groups].
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int VPL, int MAXT>
+__global__ void __launch_bounds__(MAXT) k_straddle(const KParams p) {
+  constexpr int E = Elem<T>::E;
+  extern __shared__ float sm[];
+  float* part_lo = sm;
+  float* part_hi = sm + p.nvec;
+  float* nf_s = sm + 2 * p.nvec;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  const int64_t gs = p.gs;
+  for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x) {
+    const int64_t row = item / p.chunks_per_row;
+    const int64_t c0 = (item - row * p.chunks_per_row) * p.chunk_elems;  // first column
+    const int64_t clen = min(p.chunk_elems, p.width - c0);
+    const int nv = static_cast<int>((clen + E - 1) / E);
+    const int ng = static_cast<int>(clen / gs);
+    const T* yp = static_cast<const T*>(p.y) + row * p.ys + c0;
+    const T* gp = static_cast<const T*>(p.gate) + row * p.gts + c0;
+
+    float a[VPL][E];
+    float sg[MODE == kOnnx ? VPL : 1][E];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * nthreads + tid;
+      const int64_t e0 = (int64_t)v * E;
+      float yf[E], gf[E];
+      if (v < nv && e0 + E <= clen) {
+        Elem<T>::unpack(ld_stream(yp + e0), yf);
+        Elem<T>::unpack(ld_stream(gp + e0), gf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const bool ok = v < nv && e0 + e < clen;
+          yf[e] = ok ? Elem<T>::load1(yp, e0 + e) : 0.0f;
+          gf[e] = ok ? Elem<T>::load1(gp, e0 + e) : 0.0f;
+        }
+      }
+      float lo = 0.0f, hi = 0.0f;
+      // elements [0, b) of this vector belong to group e0 / gs, the rest to the next
+      const int64_t b = ((e0 / gs) + 1) * gs - e0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (MODE == kMamba2) {
+          a[k][e] = yf[e] * silu<T>(gf[e]);
+        } else {
+          a[k][e] = yf[e];
+          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
+        }
+        if (e < b) lo = fmaf(a[k][e], a[k][e], lo);
+        else hi = fmaf(a[k][e], a[k][e], hi);
+      }
+      if (v < nv) {
+        part_lo[v] = lo;
+        part_hi[v] = hi;
+      }
+    }
+    __syncthreads();
+    for (int t = tid; t < ng; t += nthreads) {
+      const int64_t first = (int64_t)t * gs;
+      const int vf = static_cast<int>(first / E);
+      const int vl = static_cast<int>((first + gs - 1) / E);
+      float m2 = ((int64_t)vf * E >= first) ? part_lo[vf] : part_hi[vf];
+      for (int v = vf + 1; v <= vl; ++v) m2 += part_lo[v];
+      nf_s[t] = normaliser(m2, p.gs_f, p.eps);
+    }
+    __syncthreads();
+
+    T* op = static_cast<T*>(p.out) + row * p.os + c0;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * nthreads + tid;
+      if (v < nv) {
+        const int64_t e0 = (int64_t)v * E;
+        const int64_t glo = e0 / gs;
+        const int64_t b = (glo + 1) * gs - e0;
+        const float nf_lo = nf_s[glo];
+        const float nf_hi = (b < E && glo + 1 < ng) ? nf_s[glo + 1] : nf_lo;
+        float r[E];
+        if (MODE == kMamba2) {
+          float wv[E];
+          if (e0 + E <= clen) {
+            load_weight_vec<T, MODE>(p.w, c0 + e0, wv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+              wv[e] = (e0 + e < clen) ? __ldg(static_cast<const float*>(p.w) + c0 + e0 + e) : 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) r[e] = a[k][e] * (e < b ? nf_lo : nf_hi);
+#pragma unroll
+          for (int e = 0; e < E; e += 2) Elem<T>::round_pair(r[e], r[e + 1]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) r[e] = wv[e] * r[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int64_t j = (e < b) ? (e0 + e - glo * gs) : (e0 + e - (glo + 1) * gs);
+            const float sc = (e0 + e < clen) ? Elem<T>::load1(p.w, j) : 0.0f;
+            r[e] = ((a[k][e] * (e < b ? nf_lo : nf_hi)) * sc) * sg[MODE == kOnnx ? k : 0][e];
+          }
+        }
+        if (e0 + E <= clen) {
+          st_stream(op + e0, Elem<T>::pack(r));
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (e0 + e < clen) Elem<T>::store1(op, e0 + e, r[e]);
+        }
+      }
+    }
+    __syncthreads();  // shared partials are rewritten by the next chunk
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SCALAR: LANES lanes per group, element loads (any alignment, any size),
+// two passes over the group: sum of squares, then recompute and store.
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int LANES>
+__global__ void __launch_bounds__(256) k_scalar(const KParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int lane = threadIdx.x & (LANES - 1);
+  const int teams_per_warp = 32 / LANES;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int team_in_warp = (threadIdx.x & 31) / LANES;
+
+  for (int64_t base = warp_id * teams_per_warp; base < p.items;
+       base += warps_total * teams_per_warp) {
+    const int64_t item = base + team_in_warp;
+    const bool active = item < p.items;
+    int64_t row = 0, g = 0;
+    if (active) {
+      row = item / p.groups;
+      g = item - row * p.groups;
+    }
+    const int64_t col0 = g * p.gs;
+    const int64_t yo = row * p.ys + col0, go = row * p.gts + col0, oo = row * p.os + col0;
+    float ss = 0.0f;
+    if (active) {
+      for (int64_t j = lane; j < p.gs; j += LANES) {
+        const float y = Elem<T>::load1(p.y, yo + j);
+        float a = y;
+        if (MODE == kMamba2) a = y * silu<T>(Elem<T>::load1(p.gate, go + j));
+        ss = fmaf(a, a, ss);
+      }
+    }
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float nf = normaliser(ss, p.gs_f, p.eps);
+    if (active) {
+      for (int64_t j = lane; j < p.gs; j += LANES) {
+        const float y = Elem<T>::load1(p.y, yo + j);
+        const float sgv = silu<T>(Elem<T>::load1(p.gate, go + j));
+        float r;
+        if (MODE == kMamba2) {
+          float t = (y * sgv) * nf;
+          float dummy = 0.0f;
+          Elem<T>::round_pair(t, dummy);
+          r = __ldg(static_cast<const float*>(p.w) + col0 + j) * t;
+        } else {
+          r = ((y * nf) * Elem<T>::load1(p.w, j)) * sgv;
+        }
+        Elem<T>::store1(p.out, oo + j, r);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launch of the kernel a plan names, for one element type.
+// ---------------------------------------------------------------------------
+template <typename K>
+cudaError_t launch_kernel(K kernel, const KParams& k, const Plan& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(p.block));
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, k);
+}
+
+template <typename T, int MODE>
+cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
+  switch (p.path) {
+    case kTeam:
+      if (p.vpl == 1) {
+        switch (p.lanes) {
+          case 1: return launch_kernel(k_team<T, MODE, 1, 1>, k, p, s);
+          case 2: return launch_kernel(k_team<T, MODE, 2, 1>, k, p, s);
+          case 4: return launch_kernel(k_team<T, MODE, 4, 1>, k, p, s);
+          case 8: return launch_kernel(k_team<T, MODE, 8, 1>, k, p, s);
+          case 16: return launch_kernel(k_team<T, MODE, 16, 1>, k, p, s);
+          case 32: return launch_kernel(k_team<T, MODE, 32, 1>, k, p, s);
+          default: break;
+        }
+      } else if (p.lanes == 32) {
+        switch (p.vpl) {
+          case 2: return launch_kernel(k_team<T, MODE, 32, 2>, k, p, s);
+          case 4: return launch_kernel(k_team<T, MODE, 32, 4>, k, p, s);
+          default: break;
+        }
+      }
+      break;
+    case kWide:
+      if (p.vpl == 4 && p.block <= 256) return launch_kernel(k_wide<T, MODE, 4, 256>, k, p, s);
+      if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 1024>, k, p, s);
+      break;
+    case kStraddle:
+      if (p.vpl == 4 && p.block <= 256) return launch_kernel(k_straddle<T, MODE, 4, 256>, k, p, s);
+      break;
+    case kScalar:
+      if (p.lanes == 1) return launch_kernel(k_scalar<T, MODE, 1>, k, p, s);
+      if (p.lanes == 32) return launch_kernel(k_scalar<T, MODE, 32>, k, p, s);
+      break;
+    default:
+      break;
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace ggrn

@@ -1,0 +1,184 @@
+/*
+ * ggrn.h -- C ABI of the GB300 (sm_103a) fused gated group-RMSNorm library.
+ *
+ * The operation.  For every row n and every contiguous group g of
+ * group_size columns (col = g * group_size + j, 0 <= j < group_size):
+ *
+ *   GGRN_MODE_MAMBA2 -- "gated_group_rmsnorm" Mojo module page, math block
+ *   (norm_before_gate=False branch of the Mamba-2 mixer norm):
+ *       gated = f32(y[n,col]) * silu(f32(gate[n,col]))
+ *       m2    = sum_j gated^2                     (f32, over the group)
+ *       nf    = rsqrt(m2 / group_size + eps)
+ *       out[n,col] = cast_T( f32(w[col]) * f32(cast_T(gated * nf)) )
+ *     w: float32, length width, indexed by col.  T in {f32, f16, bf16}.
+ *
+ *   GGRN_MODE_ONNX -- "com.microsoft.GatedRMSNorm" README, Description and
+ *   Type constraints:
+ *       Y = X * rsqrt(mean(X^2) + eps) * scale * SiLU(gate)
+ *     mean over each contiguous group of C = group_size elements, scale of
+ *     type T and length C shared by all groups and rows, every intermediate
+ *     f32, only the store narrows.  T in {f32, f16} (bf16 is rejected).
+ *     Leading axes of X are folded into rows (rows = numel / width).
+ *
+ * Memory.  Every pointer is a DEVICE pointer owned by the caller.  y, gate
+ * and out are [rows, width] matrices of T with unit inner stride and the
+ * given row strides in ELEMENTS (a strided view split from a fused in-proj
+ * output is read in place).  The library allocates no device memory, does
+ * not synchronise, and enqueues all work on `cuda_stream` (a cudaStream_t;
+ * NULL = the legacy default stream), so calls may be captured in a CUDA
+ * graph.  out must not overlap y or gate.
+ *
+ * Errors.  Argument errors are detected on the host before anything is
+ * enqueued and returned synchronously (nothing is launched).  A launch
+ * failure returns GGRN_ERR_CUDA.  Faults inside a kernel surface, as usual
+ * for CUDA, at the next synchronising call of the caller.
+ *
+ * Numerics.  f32 arithmetic and accumulation as the pages state; the group
+ * sum is a tree (warp butterflies), not the sequential order, so a 16-bit
+ * result may differ from a sequential-order evaluation by one ulp (two in
+ * MAMBA2 when the intermediate cast flips).  Results are deterministic:
+ * identical inputs give identical bits on every call.
+ */
+#ifndef GGRN_H
+#define GGRN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GGRN_OK = 0,
+  GGRN_ERR_NULL = 1,        /* a required pointer is NULL (checked only when rows > 0) */
+  GGRN_ERR_SHAPE = 2,       /* rows < 0, width <= 0, group_size <= 0, width % group_size != 0,
+                               a row stride < width (rows > 1), or a size that overflows int64 */
+  GGRN_ERR_ALIGN = 3,       /* a forced vector path was given pointers/strides it cannot load
+                               with 16-byte vectors (automatic selection never returns this:
+                               it falls back to the scalar path) */
+  GGRN_ERR_DTYPE = 4,       /* unknown dtype or mode, or MODE_ONNX with BF16 */
+  GGRN_ERR_OVERLAP = 5,     /* the address range of out intersects that of y or gate */
+  GGRN_ERR_CUDA = 6,        /* a CUDA runtime call (launch, query) failed */
+  GGRN_ERR_UNSUPPORTED = 7, /* a forced path does not cover this shape */
+  GGRN_ERR_ARG = 8          /* an invalid path id, a NULL out-parameter, or a bad call list */
+} ggrn_status;
+
+typedef enum { GGRN_F32 = 0, GGRN_F16 = 1, GGRN_BF16 = 2 } ggrn_dtype; /* T of y, gate, out */
+
+typedef enum { GGRN_MODE_MAMBA2 = 0, GGRN_MODE_ONNX = 1 } ggrn_mode;
+
+/* Kernel families.  AUTO lets the library choose (the normal case). */
+typedef enum {
+  GGRN_PATH_AUTO = 0,
+  GGRN_PATH_TEAM = 1,     /* a team of 1..32 lanes of one warp per group, group held in
+                             registers, segmented butterfly; several groups per warp when
+                             the team is narrower than a warp (narrow and medium groups) */
+  GGRN_PATH_WIDE = 2,     /* one CTA per group, group held in registers across the CTA,
+                             warp partials combined through shared memory (wide groups) */
+  GGRN_PATH_STRADDLE = 3, /* one CTA per row (or row chunk); 16-byte vectors that straddle
+                             group boundaries; per-vector partial sums combined per group
+                             through shared memory (group_size not a multiple of the vector) */
+  GGRN_PATH_SCALAR = 4    /* element loads, any alignment and any group size; the group is
+                             read twice (a correctness path for layouts the vector paths
+                             cannot load) */
+} ggrn_path;
+
+/*
+ * ggrn_forward -- enqueue the fused gated group-RMSNorm on `cuda_stream`.
+ *   y, gate   : const T*, [rows, width], row strides y_row_stride,
+ *               gate_row_stride (elements, >= width when rows > 1).
+ *   w         : MAMBA2: const float* [width];  ONNX: const T* [group_size].
+ *   out       : T*, [rows, width], row stride out_row_stride (elements).
+ *   rows      : >= 0; rows == 0 returns GGRN_OK and launches nothing.
+ *   width     : > 0, a multiple of group_size.
+ *   group_size: > 0 (any value; no relation to the warp or vector width).
+ *   eps       : added to the mean of squares (no default; pass it).
+ *   dtype     : ggrn_dtype of y, gate, out (and scale in ONNX mode).
+ *   mode      : ggrn_mode.
+ * Returns a ggrn_status.
+ */
+int ggrn_forward(const void* y, const void* gate, const void* w, void* out, int64_t rows,
+                 int64_t width, int64_t group_size, int64_t y_row_stride,
+                 int64_t gate_row_stride, int64_t out_row_stride, float eps, int dtype,
+                 int mode, void* cuda_stream);
+
+/*
+ * ggrn_forward_path -- ggrn_forward with the kernel family forced (tests and
+ * tuning).  Same arguments plus `path` (ggrn_path).  Returns
+ * GGRN_ERR_UNSUPPORTED when the family cannot compute this shape and
+ * GGRN_ERR_ALIGN when it cannot load these pointers/strides.
+ */
+int ggrn_forward_path(const void* y, const void* gate, const void* w, void* out, int64_t rows,
+                      int64_t width, int64_t group_size, int64_t y_row_stride,
+                      int64_t gate_row_stride, int64_t out_row_stride, float eps, int dtype,
+                      int mode, int path, void* cuda_stream);
+
+/* What a call would launch (host only: launches nothing, dereferences no pointer). */
+typedef struct {
+  int32_t path;            /* ggrn_path chosen */
+  int32_t team_lanes;      /* TEAM: lanes per group; WIDE/STRADDLE: threads per CTA */
+  int32_t vec_per_lane;    /* 16-byte vectors (TEAM/WIDE/STRADDLE) each lane holds per tensor */
+  int32_t elems_per_vec;   /* elements per 16-byte vector (16 / sizeof(T)); 1 on SCALAR */
+  int64_t grid_blocks;     /* CTAs launched */
+  int32_t block_threads;   /* threads per CTA */
+  int32_t smem_bytes;      /* dynamic shared memory per CTA */
+  int64_t items;           /* work items: groups (TEAM/WIDE/SCALAR) or row chunks (STRADDLE) */
+} ggrn_plan_info;
+
+/*
+ * ggrn_plan -- fill `info` with the launch that ggrn_forward_path(..., path)
+ * would make for these arguments (path = GGRN_PATH_AUTO for ggrn_forward).
+ * Pointers are only inspected for alignment.  Validation is the same as in
+ * ggrn_forward, except that rows == 0 still yields a plan (with 0 blocks) and
+ * out may be NULL (an output not allocated yet; NULL counts as 16-byte
+ * aligned).
+ * The SM count used for grid sizing is the one of the current device when
+ * a GPU is present, else 152.
+ */
+int ggrn_plan(const void* y, const void* gate, const void* w, const void* out, int64_t rows,
+              int64_t width, int64_t group_size, int64_t y_row_stride,
+              int64_t gate_row_stride, int64_t out_row_stride, int dtype, int mode,
+              int path, ggrn_plan_info* info);
+
+/* One call of a decode chain (the arguments of ggrn_forward without the stream). */
+typedef struct {
+  const void* y;
+  const void* gate;
+  const void* w;
+  void* out;
+  int64_t rows, width, group_size;
+  int64_t y_row_stride, gate_row_stride, out_row_stride;
+  float eps;
+  int32_t dtype, mode;
+} ggrn_call;
+
+/*
+ * Decode graphs -- batch-1 decode is launch-bound (one call per layer per
+ * token; the work is a few thousand elements), so a chain of calls is
+ * captured once into a CUDA graph and replayed with one launch.
+ *
+ * ggrn_graph_create: validates every call (as ggrn_forward does), captures
+ *   the n calls in order on a private stream, and instantiates the graph.
+ *   Buffers are baked into the graph: the caller keeps them alive and
+ *   refills them in place between replays.  *graph receives an opaque
+ *   handle.  Host memory is allocated for the handle and the graph; no
+ *   device memory is allocated by this library.
+ * ggrn_graph_launch: one cudaGraphLaunch of the chain on `cuda_stream`.
+ * ggrn_graph_destroy: frees the handle (NULL is a no-op).  The caller must
+ *   make sure no launch of it is still running on the GPU.
+ */
+int ggrn_graph_create(const ggrn_call* calls, int32_t n, void** graph);
+int ggrn_graph_launch(void* graph, void* cuda_stream);
+int ggrn_graph_destroy(void* graph);
+
+/* Static description of a status code (never NULL). */
+const char* ggrn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ggrn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GGRN_H */

@@ -1,0 +1,142 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every symbol the
+header declares, validates arguments before enqueuing anything, and selects
+kernel families as designed."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_group_rmsnorm_gb300 as g
+from gated_group_rmsnorm_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(inc, fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ggrn_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return g.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared == set(binding.EXPORTS), declared ^ set(binding.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ggrn_version() >= 100
+    for st in range(9):
+        assert g.status_string(st)
+    assert g.status_string(99) == "unknown status"
+
+
+# Fake, 256-byte aligned "device" addresses: validation never dereferences them.
+Y, GATE, W, OUT = 0x10000, 0x200000, 0x300000, 0x400000
+
+
+def _fwd(*, y=Y, gate=GATE, w=W, out=OUT, rows=4, width=16, gs=8, ys=16, gts=16, os_=16,
+         dtype=2, mode=0, path=0):
+    return g.ggrn_forward_path(y, gate, w, out, rows, width, gs, ys, gts, os_, 1e-5, dtype, mode,
+                               path, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(width=16, gs=3), binding.ERR_SHAPE),
+    (dict(gs=0), binding.ERR_SHAPE),
+    (dict(width=0), binding.ERR_SHAPE),
+    (dict(rows=-1), binding.ERR_SHAPE),
+    (dict(ys=15), binding.ERR_SHAPE),
+    (dict(os_=8), binding.ERR_SHAPE),
+    (dict(rows=1 << 62, ys=1 << 40, gts=1 << 40, os_=1 << 40), binding.ERR_SHAPE),
+    (dict(y=0), binding.ERR_NULL),
+    (dict(out=0), binding.ERR_NULL),
+    (dict(w=0), binding.ERR_NULL),
+    (dict(dtype=2, mode=1), binding.ERR_DTYPE),
+    (dict(dtype=3), binding.ERR_DTYPE),
+    (dict(mode=2), binding.ERR_DTYPE),
+    (dict(y=Y + 1), binding.ERR_ALIGN),
+    (dict(w=W + 2), binding.ERR_ALIGN),
+    (dict(out=Y + 8), binding.ERR_OVERLAP),
+    (dict(out=GATE - 2), binding.ERR_OVERLAP),
+    (dict(out=W), binding.ERR_OVERLAP),
+    (dict(path=9), binding.ERR_ARG),
+    (dict(path=1, width=24, gs=12, ys=24, gts=24, os_=24), binding.ERR_UNSUPPORTED),  # TEAM: gs % 8
+    (dict(path=3, gs=8), binding.ERR_UNSUPPORTED),              # STRADDLE needs gs % 8 != 0
+    (dict(path=1, y=Y + 2), binding.ERR_ALIGN),                 # vector path, unaligned pointer
+    (dict(path=2, ys=20, gts=20, os_=20), binding.ERR_ALIGN),    # vector path, unaligned stride
+])
+def test_validation_rejects_before_launch(kwargs, status):
+    assert _fwd(**kwargs) == status
+
+
+def test_rows_zero_is_a_no_op():
+    assert _fwd(rows=0, y=0, gate=0, w=0, out=0) == binding.OK
+
+
+def test_graph_create_rejects_bad_calls(lib):
+    handle = ctypes.c_void_p()
+    assert lib.ggrn_graph_create(None, 1, ctypes.byref(handle)) == binding.ERR_ARG
+    calls = (binding.Call * 1)()
+    calls[0] = binding.Call(Y, GATE, W, OUT, 4, 16, 3, 16, 16, 16, 1e-5, 2, 0)
+    assert lib.ggrn_graph_create(calls, 1, ctypes.byref(handle)) == binding.ERR_SHAPE
+    assert lib.ggrn_graph_destroy(None) == binding.OK
+
+
+def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
+    es = 4 if dtype == 0 else 2
+    # far-apart fake addresses; out = NULL (not allocated yet) is allowed here
+    st, info = g.ggrn_plan((1 << 40) + off * es, (2 << 40) + off * es, 3 << 40, 0, rows, width,
+                           gs, ys or width, ys or width, width, dtype, mode, path)
+    assert st == binding.OK, g.status_string(st)
+    return info
+
+
+def test_plan_selects_families():
+    # Mamba-2 prefill 4096x7680, group 960 (120 vectors): one warp per group, 4 vectors/lane
+    p = _plan(4096, 7680, 960, 2)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
+    # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 16-lane teams, 2 groups per warp
+    p = _plan(32768, 4096, 128, 1, mode=1)
+    assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 16, 1)
+    # wide single group of 5120 (640 vectors): one 160-thread CTA per group
+    p = _plan(16384, 5120, 5120, 2)
+    assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
+    # odd span 100 at row stride 9664: straddling vectors, one CTA per row
+    p = _plan(65536, 4800, 100, 2, ys=9664)
+    assert (p.path, p.block_threads, p.items) == (g.PATH_STRADDLE, 160, 65536)
+    # decode (one row, 8 groups): one warp per CTA spreads the groups over SMs
+    p = _plan(1, 7680, 960, 2)
+    assert (p.path, p.block_threads, p.grid_blocks) == (g.PATH_TEAM, 32, 8)
+    # tiny groups and misaligned views fall back to element loads
+    assert _plan(8, 12, 3, 2).path == g.PATH_SCALAR
+    assert _plan(8, 960, 960, 2, off=1).path == g.PATH_SCALAR
+    assert _plan(8, 960, 960, 2, ys=961).path == g.PATH_SCALAR
+    # f32: 4 elements per vector
+    p = _plan(8, 128, 128, 0)
+    assert (p.path, p.elems_per_vec, p.team_lanes) == (g.PATH_TEAM, 4, 32)
+    # a group too wide for registers goes to the scalar two-pass path
+    assert _plan(2, 1 << 16, 1 << 16, 2).path == g.PATH_SCALAR
+    # rows == 0 still plans, with nothing to launch
+    assert _plan(0, 7680, 960, 2).grid_blocks == 0
+
+
+def test_binding_rejects_cpu_tensors():
+    y = torch.zeros(2, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        g.forward(y, y, torch.ones(8), group_size=4, eps=1e-5)
