@@ -333,6 +333,8 @@ def run_ours(args) -> None:
     L = g.load(build_if_missing=True)
 
     wl = ggrn_inputs.WORKLOADS[args.workload]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
     bytes_per_step = wl.algorithmic_bytes()
     n_sets = max(2, -(-4 * L2_BYTES // bytes_per_step))
     sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
@@ -476,6 +478,8 @@ def main(argv=None) -> None:
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(ggrn_inputs.WORKLOADS), default="mamba2_prefill")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's row count (small profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

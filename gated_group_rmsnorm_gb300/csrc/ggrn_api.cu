@@ -27,8 +27,8 @@ constexpr int kTeamBlock = 256;
 constexpr int kTeamMaxVec = 128;     // TEAM covers groups of up to 128 vectors
 constexpr int kWideVpl = 4;
 constexpr int kWideMaxThreads = 1024;
-constexpr int kStraddleVpl = 4;
-constexpr int kStraddleMaxThreads = 256;
+constexpr int kStraddleMaxVpl = 4;   // chunk of at most 128 vectors per warp
+constexpr int kStraddleBlock = 256;
 constexpr int kScalarBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;
 
@@ -189,27 +189,51 @@ int plan_wide(const Args& a, Plan* p) {
 int plan_straddle(const Args& a, Plan* p) {
   const int es = elem_size(a.dtype);
   const int E = 16 / es;
-  if (a.gs % E == 0 || a.gs < E) return GGRN_ERR_UNSUPPORTED;
-  const int64_t lcm = a.gs / gcd64(a.gs, E) * E;     // elements per period
+  // whole vectors only: group size above the vector and not a multiple of
+  // it, width a multiple of it (rows then start and end on vector bounds)
+  if (a.gs % E == 0 || a.gs < E || a.width % E != 0) return GGRN_ERR_UNSUPPORTED;
+  const int64_t g = gcd64(a.gs, E);
+  const int64_t lcm = a.gs / g * E;                 // elements per period
   const int64_t period_vecs = lcm / E;
-  const int64_t max_vecs = static_cast<int64_t>(kStraddleMaxThreads) * kStraddleVpl;
-  if (period_vecs > max_vecs) return GGRN_ERR_UNSUPPORTED;
+  if (period_vecs > 32 * kStraddleMaxVpl) return GGRN_ERR_UNSUPPORTED;
+  // Choose vectors per lane and periods per chunk (one warp per chunk) for
+  // the best use of the warp's 32*VPL vector slots over a row.
+  const int64_t row_vecs = ceil_div(a.width, E);
   const int64_t periods_per_row = ceil_div(a.width, lcm);
-  const int64_t m = std::max<int64_t>(1, std::min<int64_t>(periods_per_row, max_vecs / period_vecs));
+  double best = -1.0;
+  int best_vpl = 0;
+  int64_t best_k = 0;
+  for (int vpl = 1; vpl <= kStraddleMaxVpl; vpl *= 2) {
+    const int64_t slots = 32 * vpl;
+    const int64_t kmax = std::min<int64_t>(slots / period_vecs, periods_per_row);
+    for (int64_t k = 1; k <= kmax; ++k) {
+      const int64_t chunks = ceil_div(periods_per_row, k);
+      const double use = static_cast<double>(row_vecs) / static_cast<double>(chunks * slots);
+      if (use > best + 1e-9) {
+        best = use;
+        best_vpl = vpl;
+        best_k = k;
+      }
+    }
+  }
+  if (best_vpl == 0) return GGRN_ERR_UNSUPPORTED;
   p->path = kStraddle;
   p->elems_per_vec = E;
-  p->vpl = kStraddleVpl;
-  p->chunk_elems = m * lcm;
+  p->vpl = best_vpl;
+  p->straddle_g = static_cast<int>(g);
+  p->chunk_elems = best_k * lcm;
   p->chunks_per_row = ceil_div(a.width, p->chunk_elems);
-  const int64_t nv_max = ceil_div(std::min<int64_t>(p->chunk_elems, a.width), E);
-  p->nvec = static_cast<int>(nv_max);
   p->chunk_groups = static_cast<int>(std::min<int64_t>(p->chunk_elems, a.width) / a.gs);
-  p->block = static_cast<int>(ceil_div(ceil_div(nv_max, kStraddleVpl), 32) * 32);
-  p->lanes = p->block;
+  p->nvec = static_cast<int>(ceil_div(std::min<int64_t>(p->chunk_elems, a.width), E));
+  p->gs_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(a.gs) + 1);
+  p->warp_smem = 2 * 32 * best_vpl + p->chunk_groups;
+  p->block = kStraddleBlock;
+  p->lanes = 32;
   p->groups = a.width / a.gs;
   p->items = a.rows * p->chunks_per_row;
-  p->grid = std::min<int64_t>(kMaxGrid, p->items);
-  p->smem = static_cast<int>((2 * nv_max + p->chunk_groups) * sizeof(float));
+  const int64_t warps = kStraddleBlock / 32;
+  p->grid = std::min<int64_t>(kMaxGrid, ceil_div(p->items, warps));
+  p->smem = static_cast<int>(warps * p->warp_smem * sizeof(float));
   return GGRN_OK;
 }
 
@@ -321,6 +345,8 @@ KParams make_params(const Args& a, const Plan& p) {
   k.chunks_per_row = p.chunks_per_row;
   k.nvec = p.nvec;
   k.chunk_groups = p.chunk_groups;
+  k.warp_smem = p.warp_smem;
+  k.gs_magic = p.gs_magic;
   k.eps = a.eps;
   k.gs_f = static_cast<float>(a.gs);
   return k;

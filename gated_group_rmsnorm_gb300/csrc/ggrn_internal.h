@@ -39,6 +39,9 @@ struct Plan {
   int64_t chunk_elems = 0;     // elements per chunk (a multiple of lcm(gs, E))
   int64_t chunks_per_row = 0;
   int chunk_groups = 0;        // groups per full chunk
+  int straddle_g = 0;          // gcd(gs, E)
+  uint32_t gs_magic = 0;       // floor(2^32 / gs) + 1: exact floor(x / gs) for x, gs < 2^11
+  int warp_smem = 0;           // floats of shared memory per warp
 };
 
 // Kernel parameters (passed by value).
@@ -56,6 +59,8 @@ struct KParams {
   int64_t chunks_per_row;
   int nvec;
   int chunk_groups;
+  int warp_smem;
+  uint32_t gs_magic;
   float eps;
   float gs_f;
 };

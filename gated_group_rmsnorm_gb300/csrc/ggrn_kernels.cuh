@@ -23,11 +23,11 @@
 //               groups share a warp with no shared memory and no barrier.
 //   k_wide      one CTA per group; warp butterflies, then one shared-memory
 //               exchange and one barrier.
-//   k_straddle  one CTA per row chunk holding whole groups, for group sizes
+//   k_straddle  one warp per row chunk holding whole groups, for group sizes
 //               that are not a multiple of the vector: each vector's squares
 //               are split at the (at most one) group boundary it crosses, the
-//               two partials go to shared memory, and one thread per group
-//               adds its vectors' partials in a fixed order.
+//               two partials go to warp-private shared memory, and one lane
+//               per group adds its vectors' partials in a fixed order.
 //   k_scalar    element loads, LANES lanes per group, two passes over the
 //               group (a correctness path for any alignment and size).
 //
@@ -69,8 +69,9 @@ struct Elem<float> {
   __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
     static_cast<float*>(p)[i] = v;
   }
-  // Accurate exp for f32 outputs (their tolerance is relative, 1e-5).
-  __device__ __forceinline__ static float exp_neg(float x) { return expf(-x); }
+  // f32 outputs carry a relative tolerance of 1e-5 at every magnitude: their
+  // silu uses the accurate exponential and the IEEE divide.
+  static constexpr bool kExactSilu = true;
 };
 
 template <>
@@ -101,7 +102,7 @@ struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
     static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
   }
-  __device__ __forceinline__ static float exp_neg(float x) { return __expf(-x); }
+  static constexpr bool kExactSilu = false;
 };
 
 template <>
@@ -133,7 +134,7 @@ struct Elem<__half> {
   __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
     static_cast<__half*>(p)[i] = __float2half_rn(v);
   }
-  __device__ __forceinline__ static float exp_neg(float x) { return __expf(-x); }
+  static constexpr bool kExactSilu = false;
 };
 
 // ---------------------------------------------------------------------------
@@ -170,15 +171,32 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ---------------------------------------------------------------------------
 // Math helpers.
 // ---------------------------------------------------------------------------
-// silu(b) = b / (1 + exp(-b)), f32.  The fast divide returns 0 for
-// denominators above 2^126; there the quotient is still a normal float, so
-// that (rare) case takes the IEEE divide.
+// Approximate base-2 exponential and reciprocal of the PTX ISA (one MUFU
+// operation each, subnormal results flushed to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// silu(b) = b * sigmoid(b) = b / (1 + exp(-b)), in f32.
+// 16-bit T: exp(-b) = 2^(-b * log2(e)) and the divide as a reciprocal
+// times b, two MUFU operations per element.  Numerator and denominator are
+// both scaled by 1/16 (exactly), so the reciprocal's argument stays below
+// 2^126 for every finite exponential and the quotient is never flushed: the
+// result keeps the exact limits of the definition -- b itself once
+// exp(-b) < 2^-24, -0 once exp(-b) overflows, NaN for b = -inf.
 template <typename T>
 __device__ __forceinline__ float silu(float b) {
-  const float d = 1.0f + Elem<T>::exp_neg(b);
-  float s = __fdividef(b, d);
-  if (d > 0x1p126f) s = b / d;
-  return s;
+  if (Elem<T>::kExactSilu) return b / (1.0f + expf(-b));
+  const float e = ex2_approx(b * -1.4426950408889634f);
+  const float d = fmaf(e, 0.0625f, 0.0625f);
+  return (b * 0.0625f) * rcp_approx(d);
 }
 
 // nf = rsqrt(m2 / gs + eps): IEEE divide, then a correctly rounded rsqrt
@@ -407,55 +425,76 @@ __global__ void __launch_bounds__(MAXT) k_wide(const KParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// STRADDLE: group size not a multiple of E (and larger than E).  One CTA per
-// chunk of a row: chunks start at multiples of lcm(gs, E) elements, so they
-// start 16-byte aligned and hold whole groups.  A vector then touches at most
-// two groups; its squares are split at the boundary into (lo, hi) partials.
-// Shared memory: part_lo[nvec], part_hi[nvec], nf[chunk_groups].
+// STRADDLE: group size not a multiple of E (and larger than E).  One warp
+// per chunk of a row.  Chunks start at multiples of lcm(gs, E) elements, so
+// they start 16-byte aligned, hold whole groups, and map vector slots to
+// groups identically in every chunk.  A vector touches at most two groups and
+// a group boundary falls inside it at a multiple of G = gcd(gs, E): the
+// vector's squares are summed in E/G sub-blocks, and the sub-block sums are
+// split at the boundary into (lo, hi) partials.  The partials go to
+// warp-private shared memory; lane t then adds, in vector order, the
+// partials of group t.  Shared memory per warp: part_lo[32*VPL],
+// part_hi[32*VPL], nf[chunk_groups]; no block-wide barrier.
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, int VPL, int MAXT>
-__global__ void __launch_bounds__(MAXT) k_straddle(const KParams p) {
+template <typename T, int MODE, int VPL, int G>
+__global__ void __launch_bounds__(256) k_straddle(const KParams p) {
   constexpr int E = Elem<T>::E;
+  constexpr int NS = E / G;          // sub-blocks per vector
+  constexpr int SLOTS = 32 * VPL;
   extern __shared__ float sm[];
-  float* part_lo = sm;
-  float* part_hi = sm + p.nvec;
-  float* nf_s = sm + 2 * p.nvec;
+  const int lane = threadIdx.x & 31;
+  float* part_lo = sm + (threadIdx.x >> 5) * p.warp_smem;
+  float* part_hi = part_lo + SLOTS;
+  float* nf_s = part_hi + SLOTS;
   pdl_wait();
   pdl_launch_dependents();
 
-  const int tid = threadIdx.x;
-  const int nthreads = blockDim.x;
-  const int64_t gs = p.gs;
-  for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x) {
+  const int gs = static_cast<int>(p.gs);
+  // Slot k of this lane holds chunk vector v = 32k + lane: its first element's
+  // group (floor(v*E / gs) by multiply-high with the host's magic number,
+  // exact for v*E, gs < 2^11) and the offset of the next group boundary.
+  int glo[VPL], bnd[VPL];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const int e0 = (k * 32 + lane) * E;
+    glo[k] = static_cast<int>(__umulhi(static_cast<unsigned>(e0), p.gs_magic));
+    bnd[k] = (glo[k] + 1) * gs - e0;
+  }
+
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       item < p.items; item += warps_total) {
     const int64_t row = item / p.chunks_per_row;
-    const int64_t c0 = (item - row * p.chunks_per_row) * p.chunk_elems;  // first column
-    const int64_t clen = min(p.chunk_elems, p.width - c0);
-    const int nv = static_cast<int>((clen + E - 1) / E);
-    const int ng = static_cast<int>(clen / gs);
+    const int64_t c0 = (item - row * p.chunks_per_row) * p.chunk_elems;
+    const int clen = static_cast<int>(min(p.chunk_elems, p.width - c0));
+    const int nv = clen / E;   // the width is a multiple of E: whole vectors only
+    const int ng = clen / gs;
     const T* yp = static_cast<const T*>(p.y) + row * p.ys + c0;
     const T* gp = static_cast<const T*>(p.gate) + row * p.gts + c0;
 
+    uint4 yr[VPL], gr[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int e0 = (k * 32 + lane) * E;
+      if (e0 < clen) {
+        yr[k] = ld_stream(yp + e0);
+        gr[k] = ld_stream(gp + e0);
+      } else {
+        yr[k] = make_uint4(0u, 0u, 0u, 0u);
+        gr[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     float a[VPL][E];
     float sg[MODE == kOnnx ? VPL : 1][E];
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      const int v = k * nthreads + tid;
-      const int64_t e0 = (int64_t)v * E;
+      const int v = k * 32 + lane;
       float yf[E], gf[E];
-      if (v < nv && e0 + E <= clen) {
-        Elem<T>::unpack(ld_stream(yp + e0), yf);
-        Elem<T>::unpack(ld_stream(gp + e0), gf);
-      } else {
+      Elem<T>::unpack(yr[k], yf);
+      Elem<T>::unpack(gr[k], gf);
+      float sub[NS];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const bool ok = v < nv && e0 + e < clen;
-          yf[e] = ok ? Elem<T>::load1(yp, e0 + e) : 0.0f;
-          gf[e] = ok ? Elem<T>::load1(gp, e0 + e) : 0.0f;
-        }
-      }
-      float lo = 0.0f, hi = 0.0f;
-      // elements [0, b) of this vector belong to group e0 / gs, the rest to the next
-      const int64_t b = ((e0 / gs) + 1) * gs - e0;
+      for (int i = 0; i < NS; ++i) sub[i] = 0.0f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         if (MODE == kMamba2) {
@@ -464,69 +503,64 @@ __global__ void __launch_bounds__(MAXT) k_straddle(const KParams p) {
           a[k][e] = yf[e];
           sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
         }
-        if (e < b) lo = fmaf(a[k][e], a[k][e], lo);
-        else hi = fmaf(a[k][e], a[k][e], hi);
+        sub[e / G] = fmaf(a[k][e], a[k][e], sub[e / G]);
+      }
+      float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        if (i * G < bnd[k]) lo += sub[i];
+        else hi += sub[i];
       }
       if (v < nv) {
         part_lo[v] = lo;
         part_hi[v] = hi;
       }
     }
-    __syncthreads();
-    for (int t = tid; t < ng; t += nthreads) {
-      const int64_t first = (int64_t)t * gs;
-      const int vf = static_cast<int>(first / E);
-      const int vl = static_cast<int>((first + gs - 1) / E);
-      float m2 = ((int64_t)vf * E >= first) ? part_lo[vf] : part_hi[vf];
+    __syncwarp();
+    for (int t = lane; t < ng; t += 32) {
+      const int first = t * gs;
+      const int vf = first / E;
+      const int vl = (first + gs - 1) / E;
+      float m2 = (vf * E >= first) ? part_lo[vf] : part_hi[vf];
       for (int v = vf + 1; v <= vl; ++v) m2 += part_lo[v];
       nf_s[t] = normaliser(m2, p.gs_f, p.eps);
     }
-    __syncthreads();
+    __syncwarp();
 
     T* op = static_cast<T*>(p.out) + row * p.os + c0;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      const int v = k * nthreads + tid;
+      const int v = k * 32 + lane;
+      const int e0 = v * E;
       if (v < nv) {
-        const int64_t e0 = (int64_t)v * E;
-        const int64_t glo = e0 / gs;
-        const int64_t b = (glo + 1) * gs - e0;
-        const float nf_lo = nf_s[glo];
-        const float nf_hi = (b < E && glo + 1 < ng) ? nf_s[glo + 1] : nf_lo;
+        const float nf_lo = nf_s[glo[k]];
+        const float nf_hi = (bnd[k] < E && glo[k] + 1 < ng) ? nf_s[glo[k] + 1] : nf_lo;
+        float nfv[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) nfv[i] = (i * G < bnd[k]) ? nf_lo : nf_hi;
         float r[E];
         if (MODE == kMamba2) {
           float wv[E];
-          if (e0 + E <= clen) {
-            load_weight_vec<T, MODE>(p.w, c0 + e0, wv);
-          } else {
+          load_weight_vec<T, MODE>(p.w, c0 + e0, wv);
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-              wv[e] = (e0 + e < clen) ? __ldg(static_cast<const float*>(p.w) + c0 + e0 + e) : 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < E; ++e) r[e] = a[k][e] * (e < b ? nf_lo : nf_hi);
+          for (int e = 0; e < E; ++e) r[e] = a[k][e] * nfv[e / G];
 #pragma unroll
           for (int e = 0; e < E; e += 2) Elem<T>::round_pair(r[e], r[e + 1]);
 #pragma unroll
           for (int e = 0; e < E; ++e) r[e] = wv[e] * r[e];
         } else {
+          // scale index j of each element: offset from its group's start
+          const int jlo = e0 - glo[k] * gs;
 #pragma unroll
           for (int e = 0; e < E; ++e) {
-            const int64_t j = (e < b) ? (e0 + e - glo * gs) : (e0 + e - (glo + 1) * gs);
-            const float sc = (e0 + e < clen) ? Elem<T>::load1(p.w, j) : 0.0f;
-            r[e] = ((a[k][e] * (e < b ? nf_lo : nf_hi)) * sc) * sg[MODE == kOnnx ? k : 0][e];
+            const int j = (e / G * G < bnd[k]) ? jlo + e : jlo + e - gs;
+            r[e] = ((a[k][e] * nfv[e / G]) * Elem<T>::load1(p.w, j)) * sg[MODE == kOnnx ? k : 0][e];
           }
         }
-        if (e0 + E <= clen) {
-          st_stream(op + e0, Elem<T>::pack(r));
-        } else {
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            if (e0 + e < clen) Elem<T>::store1(op, e0 + e, r[e]);
-        }
+        st_stream(op + e0, Elem<T>::pack(r));
       }
     }
-    __syncthreads();  // shared partials are rewritten by the next chunk
+    __syncwarp();  // the next chunk rewrites this warp's partials
   }
 }
 
@@ -605,6 +639,30 @@ cudaError_t launch_kernel(K kernel, const KParams& k, const Plan& p, cudaStream_
   return cudaLaunchKernelEx(&cfg, kernel, k);
 }
 
+template <typename T, int MODE, int G>
+cudaError_t launch_straddle_g(const KParams& k, const Plan& p, cudaStream_t s) {
+  switch (p.vpl) {
+    case 1: return launch_kernel(k_straddle<T, MODE, 1, G>, k, p, s);
+    case 2: return launch_kernel(k_straddle<T, MODE, 2, G>, k, p, s);
+    case 4: return launch_kernel(k_straddle<T, MODE, 4, G>, k, p, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <typename T, int MODE>
+cudaError_t launch_straddle(const KParams& k, const Plan& p, cudaStream_t s) {
+  // G = gcd(group size, E) < E
+  switch (p.straddle_g) {
+    case 1: return launch_straddle_g<T, MODE, 1>(k, p, s);
+    case 2: return launch_straddle_g<T, MODE, 2>(k, p, s);
+    case 4:
+      if (Elem<T>::E > 4) return launch_straddle_g<T, MODE, (Elem<T>::E > 4 ? 4 : 2)>(k, p, s);
+      break;
+    default: break;
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
 template <typename T, int MODE>
 cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
   switch (p.path) {
@@ -632,8 +690,7 @@ cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
       if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 1024>, k, p, s);
       break;
     case kStraddle:
-      if (p.vpl == 4 && p.block <= 256) return launch_kernel(k_straddle<T, MODE, 4, 256>, k, p, s);
-      break;
+      return launch_straddle<T, MODE>(k, p, s);
     case kScalar:
       if (p.lanes == 1) return launch_kernel(k_scalar<T, MODE, 1>, k, p, s);
       if (p.lanes == 32) return launch_kernel(k_scalar<T, MODE, 32>, k, p, s);

@@ -117,9 +117,13 @@ def test_plan_selects_families():
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
-    # odd span 100 at row stride 9664: straddling vectors, one CTA per row
+    # odd span 100 at row stride 9664: straddling vectors; one warp per chunk
+    # of 5 periods (lcm(100, 8) = 200 elements = 25 vectors) in 128 slots,
+    # 5 chunks per row
     p = _plan(65536, 4800, 100, 2, ys=9664)
-    assert (p.path, p.block_threads, p.items) == (g.PATH_STRADDLE, 160, 65536)
+    assert (p.path, p.block_threads, p.vec_per_lane, p.items) == (g.PATH_STRADDLE, 256, 4, 5 * 65536)
+    # a width that is not a multiple of the vector goes to the scalar path
+    assert _plan(4, 300, 100, 2).path == g.PATH_SCALAR
     # decode (one row, 8 groups): one warp per CTA spreads the groups over SMs
     p = _plan(1, 7680, 960, 2)
     assert (p.path, p.block_threads, p.grid_blocks) == (g.PATH_TEAM, 32, 8)
