@@ -133,6 +133,14 @@ int next_pow2(int v) {
   return p;
 }
 
+// Multiplier for the kernels' floor(item / d) (see div_by in
+// ggrn_kernels.cuh): floor(2^64 / d) + 1, valid while every item index is
+// below 2^32; 0 (plain division) otherwise or for d < 2.
+uint64_t div_magic(int64_t items, int64_t d) {
+  if (d < 2 || items > static_cast<int64_t>(UINT32_MAX)) return 0;
+  return UINT64_MAX / static_cast<uint64_t>(d) + 1;
+}
+
 // One item per team or CTA; grid capped at the launch limit (the kernels
 // stride over the remaining items).
 int plan_team(const Args& a, Plan* p) {
@@ -144,15 +152,14 @@ int plan_team(const Args& a, Plan* p) {
   p->path = kTeam;
   p->elems_per_vec = E;
   p->nvec = static_cast<int>(nvec);
-  if (nvec <= 32) {
-    p->lanes = next_pow2(static_cast<int>(nvec));
-    p->vpl = 1;
-  } else {
-    p->lanes = 32;
-    p->vpl = nvec <= 64 ? 2 : 4;
-  }
+  // Four vectors per lane (fewer for tiny groups) and as many lanes as that
+  // needs: the per-group costs (indexing, butterfly, normaliser) then spread
+  // over at least 32 elements per lane, and a warp serves 32/lanes groups.
+  p->vpl = nvec >= 4 ? 4 : next_pow2(static_cast<int>(nvec));
+  p->lanes = next_pow2(static_cast<int>(ceil_div(nvec, p->vpl)));
   p->groups = a.width / a.gs;
   p->items = a.rows * p->groups;
+  p->div_magic = div_magic(p->items, p->groups);
   // Spread small problems over the SMs: shrink the block (down to one warp)
   // while that keeps the grid under one CTA per SM.
   const int sms = sm_count();
@@ -181,6 +188,7 @@ int plan_wide(const Args& a, Plan* p) {
   p->block = static_cast<int>(threads);
   p->groups = a.width / a.gs;
   p->items = a.rows * p->groups;
+  p->div_magic = div_magic(p->items, p->groups);
   p->grid = std::min<int64_t>(kMaxGrid, p->items);
   p->smem = 0;
   return GGRN_OK;
@@ -231,6 +239,7 @@ int plan_straddle(const Args& a, Plan* p) {
   p->lanes = 32;
   p->groups = a.width / a.gs;
   p->items = a.rows * p->chunks_per_row;
+  p->div_magic = div_magic(p->items, p->chunks_per_row);
   const int64_t warps = kStraddleBlock / 32;
   p->grid = std::min<int64_t>(kMaxGrid, ceil_div(p->items, warps));
   p->smem = static_cast<int>(warps * p->warp_smem * sizeof(float));
@@ -244,6 +253,7 @@ int plan_scalar(const Args& a, Plan* p) {
   p->lanes = a.gs <= 16 ? 1 : 32;
   p->groups = a.width / a.gs;
   p->items = a.rows * p->groups;
+  p->div_magic = div_magic(p->items, p->groups);
   p->block = kScalarBlock;
   const int64_t teams_per_block = (kScalarBlock / 32) * (32 / p->lanes);
   p->grid = std::min<int64_t>(kMaxGrid, ceil_div(p->items, teams_per_block));
@@ -347,6 +357,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.chunk_groups = p.chunk_groups;
   k.warp_smem = p.warp_smem;
   k.gs_magic = p.gs_magic;
+  k.div_magic = p.div_magic;
   k.eps = a.eps;
   k.gs_f = static_cast<float>(a.gs);
   return k;

@@ -42,6 +42,7 @@ struct Plan {
   int straddle_g = 0;          // gcd(gs, E)
   uint32_t gs_magic = 0;       // floor(2^32 / gs) + 1: exact floor(x / gs) for x, gs < 2^11
   int warp_smem = 0;           // floats of shared memory per warp
+  uint64_t div_magic = 0;      // floor(2^64 / items_per_row) + 1, or 0 (see div_by)
 };
 
 // Kernel parameters (passed by value).
@@ -61,6 +62,7 @@ struct KParams {
   int chunk_groups;
   int warp_smem;
   uint32_t gs_magic;
+  uint64_t div_magic;
   float eps;
   float gs_f;
 };

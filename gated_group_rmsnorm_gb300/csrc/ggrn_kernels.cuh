@@ -199,6 +199,18 @@ __device__ __forceinline__ float silu(float b) {
   return (b * 0.0625f) * rcp_approx(d);
 }
 
+// floor(n / d) for the work-item counters (row = item / items_per_row).  The
+// host passes magic = floor(2^64 / d) + 1 when every n is below 2^32: then
+// n * magic / 2^64 exceeds n / d by less than 2^-32 <= 1/d, which cannot
+// carry past the next integer, so the high word of the product is the exact
+// quotient (division by an invariant integer, Granlund and Montgomery 1994).
+// magic == 0 selects the plain 64-bit division.
+__device__ __forceinline__ int64_t div_by(int64_t n, int64_t d, uint64_t magic) {
+  if (d == 1) return n;
+  if (magic != 0) return static_cast<int64_t>(__umul64hi(static_cast<uint64_t>(n), magic));
+  return n / d;
+}
+
 // nf = rsqrt(m2 / gs + eps): IEEE divide, then a correctly rounded rsqrt
 // (once per group, so the exact forms cost nothing).
 __device__ __forceinline__ float normaliser(float m2, float gs_f, float eps) {
@@ -261,7 +273,7 @@ __device__ __forceinline__ void load_weight_vec(const void* w, int64_t idx, floa
 // butterfly with offsets < LANES never crosses a segment.
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, int LANES, int VPL>
-__global__ void __launch_bounds__(256) k_team(const KParams p) {
+__global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
   constexpr int E = Elem<T>::E;
   pdl_wait();
   pdl_launch_dependents();
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(256) k_team(const KParams p) {
     const bool active = item < p.items;
     int64_t row = 0, g = 0;
     if (active) {
-      row = item / p.groups;
+      row = div_by(item, p.groups, p.div_magic);
       g = item - row * p.groups;
     }
     const int64_t col0 = g * p.gs;
@@ -298,24 +310,25 @@ __global__ void __launch_bounds__(256) k_team(const KParams p) {
       }
     }
 
-    float a[VPL][E];   // MAMBA2: gated; ONNX: x
-    float sg[MODE == kOnnx ? VPL : 1][E];
+    // MAMBA2: a = gated = y * silu(gate).  ONNX: a = x; the gate enters only
+    // the epilogue, so its raw bits wait there and silu is evaluated once.
+    float a[VPL][E];
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      float yf[E], gf[E];
+      float yf[E];
       Elem<T>::unpack(yr[k], yf);
-      Elem<T>::unpack(gr[k], gf);
+      if (MODE == kMamba2) {
+        float gf[E];
+        Elem<T>::unpack(gr[k], gf);
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        if (MODE == kMamba2) {
-          a[k][e] = yf[e] * silu<T>(gf[e]);
-        } else {
-          a[k][e] = yf[e];
-          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
-        }
-        ss = fmaf(a[k][e], a[k][e], ss);
+        for (int e = 0; e < E; ++e) a[k][e] = yf[e] * silu<T>(gf[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[k][e] = yf[e];
       }
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(a[k][e], a[k][e], ss);
     }
 #pragma unroll
     for (int o = LANES / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -333,7 +346,11 @@ __global__ void __launch_bounds__(256) k_team(const KParams p) {
           o = epilogue_mamba2<T>(a[k], nf, wv);
         } else {
           load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
-          o = epilogue_onnx<T>(a[k], sg[MODE == kOnnx ? k : 0], nf, wv);
+          float gf[E], sg[E];
+          Elem<T>::unpack(gr[k], gf);
+#pragma unroll
+          for (int e = 0; e < E; ++e) sg[e] = silu<T>(gf[e]);
+          o = epilogue_onnx<T>(a[k], sg, nf, wv);
         }
         st_stream(op + (int64_t)v * E, o);
       }
@@ -348,7 +365,7 @@ __global__ void __launch_bounds__(256) k_team(const KParams p) {
 // every thread adds them in the same order.
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, int VPL, int MAXT>
-__global__ void __launch_bounds__(MAXT) k_wide(const KParams p) {
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParams p) {
   constexpr int E = Elem<T>::E;
   __shared__ float red[2][32];
   pdl_wait();
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(MAXT) k_wide(const KParams p) {
   const int nwarps = nthreads >> 5;
   int parity = 0;
   for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x, parity ^= 1) {
-    const int64_t row = item / p.groups;
+    const int64_t row = div_by(item, p.groups, p.div_magic);
     const int64_t g = item - row * p.groups;
     const int64_t col0 = g * p.gs;
     const T* yp = static_cast<const T*>(p.y) + row * p.ys + col0;
@@ -437,7 +454,7 @@ __global__ void __launch_bounds__(MAXT) k_wide(const KParams p) {
 // part_hi[32*VPL], nf[chunk_groups]; no block-wide barrier.
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, int VPL, int G>
-__global__ void __launch_bounds__(256) k_straddle(const KParams p) {
+__global__ void __launch_bounds__(256, 3) k_straddle(const KParams p) {
   constexpr int E = Elem<T>::E;
   constexpr int NS = E / G;          // sub-blocks per vector
   constexpr int SLOTS = 32 * VPL;
@@ -464,7 +481,7 @@ __global__ void __launch_bounds__(256) k_straddle(const KParams p) {
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
        item < p.items; item += warps_total) {
-    const int64_t row = item / p.chunks_per_row;
+    const int64_t row = div_by(item, p.chunks_per_row, p.div_magic);
     const int64_t c0 = (item - row * p.chunks_per_row) * p.chunk_elems;
     const int clen = static_cast<int>(min(p.chunk_elems, p.width - c0));
     const int nv = clen / E;   // the width is a multiple of E: whole vectors only
@@ -585,7 +602,7 @@ __global__ void __launch_bounds__(256) k_scalar(const KParams p) {
     const bool active = item < p.items;
     int64_t row = 0, g = 0;
     if (active) {
-      row = item / p.groups;
+      row = div_by(item, p.groups, p.div_magic);
       g = item - row * p.groups;
     }
     const int64_t col0 = g * p.gs;
@@ -667,22 +684,16 @@ template <typename T, int MODE>
 cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
   switch (p.path) {
     case kTeam:
-      if (p.vpl == 1) {
-        switch (p.lanes) {
-          case 1: return launch_kernel(k_team<T, MODE, 1, 1>, k, p, s);
-          case 2: return launch_kernel(k_team<T, MODE, 2, 1>, k, p, s);
-          case 4: return launch_kernel(k_team<T, MODE, 4, 1>, k, p, s);
-          case 8: return launch_kernel(k_team<T, MODE, 8, 1>, k, p, s);
-          case 16: return launch_kernel(k_team<T, MODE, 16, 1>, k, p, s);
-          case 32: return launch_kernel(k_team<T, MODE, 32, 1>, k, p, s);
-          default: break;
-        }
-      } else if (p.lanes == 32) {
-        switch (p.vpl) {
-          case 2: return launch_kernel(k_team<T, MODE, 32, 2>, k, p, s);
-          case 4: return launch_kernel(k_team<T, MODE, 32, 4>, k, p, s);
-          default: break;
-        }
+      switch (p.lanes * 8 + p.vpl) {   // (lanes, vectors per lane) pairs the host plans
+        case 1 * 8 + 1: return launch_kernel(k_team<T, MODE, 1, 1>, k, p, s);
+        case 1 * 8 + 2: return launch_kernel(k_team<T, MODE, 1, 2>, k, p, s);
+        case 1 * 8 + 4: return launch_kernel(k_team<T, MODE, 1, 4>, k, p, s);
+        case 2 * 8 + 4: return launch_kernel(k_team<T, MODE, 2, 4>, k, p, s);
+        case 4 * 8 + 4: return launch_kernel(k_team<T, MODE, 4, 4>, k, p, s);
+        case 8 * 8 + 4: return launch_kernel(k_team<T, MODE, 8, 4>, k, p, s);
+        case 16 * 8 + 4: return launch_kernel(k_team<T, MODE, 16, 4>, k, p, s);
+        case 32 * 8 + 4: return launch_kernel(k_team<T, MODE, 32, 4>, k, p, s);
+        default: break;
       }
       break;
     case kWide:

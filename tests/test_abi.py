@@ -111,9 +111,10 @@ def test_plan_selects_families():
     # Mamba-2 prefill 4096x7680, group 960 (120 vectors): one warp per group, 4 vectors/lane
     p = _plan(4096, 7680, 960, 2)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
-    # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 16-lane teams, 2 groups per warp
+    # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 4-lane teams with 4
+    # vectors each, 8 groups per warp
     p = _plan(32768, 4096, 128, 1, mode=1)
-    assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 16, 1)
+    assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 4)
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
@@ -133,7 +134,7 @@ def test_plan_selects_families():
     assert _plan(8, 960, 960, 2, ys=961).path == g.PATH_SCALAR
     # f32: 4 elements per vector
     p = _plan(8, 128, 128, 0)
-    assert (p.path, p.elems_per_vec, p.team_lanes) == (g.PATH_TEAM, 4, 32)
+    assert (p.path, p.elems_per_vec, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 8, 4)
     # a group too wide for registers goes to the scalar two-pass path
     assert _plan(2, 1 << 16, 1 << 16, 2).path == g.PATH_SCALAR
     # rows == 0 still plans, with nothing to launch
