@@ -20,20 +20,23 @@ OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_OVERLAP, ERR_CUDA, ERR_UNSUPP
 # ggrn_dtype / ggrn_mode / ggrn_path
 F32, F16, BF16 = 0, 1, 2
 MAMBA2, ONNX = 0, 1
-PATH_AUTO, PATH_TEAM, PATH_WIDE, PATH_STRADDLE, PATH_SCALAR = range(5)
+PATH_AUTO, PATH_TEAM, PATH_WIDE, PATH_STRADDLE, PATH_SCALAR, PATH_STREAM = range(6)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_TEAM: "team", PATH_WIDE: "wide",
-              PATH_STRADDLE: "straddle", PATH_SCALAR: "scalar"}
+              PATH_STRADDLE: "straddle", PATH_SCALAR: "scalar", PATH_STREAM: "stream"}
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 
 # The exported symbols, as include/ggrn.h declares them.
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
-           "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version")
+           "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
+           "ggrn_fault_status", "ggrn_last_cuda_error")
 
 
 class GgrnError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         msg = status_string(status) if _lib is not None else f"status {status}"
+        if status == ERR_CUDA and _lib is not None:
+            msg += f" [{_lib.ggrn_last_cuda_error().decode()}]"
         super().__init__(f"{what}: {msg} (status {status})" if what else f"{msg} (status {status})")
         self.status = status
 
@@ -98,12 +101,25 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ggrn_status_string.restype = ctypes.c_char_p
         L.ggrn_version.argtypes = []
         L.ggrn_version.restype = ci
+        L.ggrn_fault_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci]
+        L.ggrn_fault_status.restype = ci
+        L.ggrn_last_cuda_error.argtypes = []
+        L.ggrn_last_cuda_error.restype = ctypes.c_char_p
         _lib = L
         return L
 
 
 def status_string(status: int) -> str:
     return load().ggrn_status_string(status).decode()
+
+
+def fault_status(clear: bool = False) -> int:
+    """The device status word (nonzero: a streaming kernel's bounded wait ran out)."""
+    flags = ctypes.c_uint32(0)
+    st = load().ggrn_fault_status(ctypes.byref(flags), 1 if clear else 0)
+    if st != OK:
+        raise GgrnError(st, "ggrn_fault_status")
+    return flags.value
 
 
 # ---------------------------------------------------------------------------

@@ -13,14 +13,37 @@
 #include <algorithm>
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/ggrn.h"
 #include "ggrn_internal.h"
 
+// Device status word of the library (one per device): kernels whose bounded
+// waits run out set bits here (see ggrn_fault_status).
+__device__ unsigned int g_ggrn_fault;
+
 namespace ggrn {
 namespace {
+
+// The CUDA error behind the last GGRN_ERR_CUDA of this thread.
+thread_local cudaError_t tl_last_cuda_error = cudaSuccess;
+
+// Address of this device's status word (looked up once per device).
+unsigned int* fault_word() {
+  static std::mutex mu;
+  static unsigned int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_ggrn_fault) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(ptr);
+  }
+  return cache[dev];
+}
 
 constexpr int kDefaultSMs = 152;
 constexpr int kTeamBlock = 256;
@@ -31,6 +54,13 @@ constexpr int kStraddleMaxVpl = 4;   // chunk of at most 128 vectors per warp
 constexpr int kStraddleBlock = 256;
 constexpr int kScalarBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;
+constexpr int kStreamWarps = 8;                 // consumer warps per CTA (target)
+constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
+// Two CTAs per SM, 8 consumer warps, a double-buffered ring: the best of a
+// sweep over 1-2 CTAs/SM, 6-16 consumer warps and 2-4 stages on the prefill
+// and gated-DeltaNet shapes (deeper rings were up to 5% slower).
+constexpr int64_t kStreamMaxStages = 2;
+constexpr int64_t kStreamMaxWeightBytes = 64 * 1024;
 
 int elem_size(int dtype) { return dtype == kF32 ? 4 : 2; }
 
@@ -262,12 +292,118 @@ int plan_scalar(const Args& a, Plan* p) {
   return GGRN_OK;
 }
 
+// STREAM: persistent CTAs fed by bulk copies of row chunks ("units" of ug
+// whole groups).  Eligible when a group's bytes are a multiple of 8, it
+// spans 4..128 shared-memory vectors, every unit is a 16-byte multiple, and
+// there are at least two units per CTA slot.
+int plan_stream(const Args& a, Plan* p, bool forced) {
+  const int es = elem_size(a.dtype);
+  const int64_t gbytes = a.gs * es;
+  const int sv = (gbytes % 16 == 0) ? 16 : (gbytes % 8 == 0 ? 8 : 0);
+  if (sv == 0) return GGRN_ERR_UNSUPPORTED;
+  const int se = sv / es;
+  const int64_t nvec = a.gs / se;
+  if (nvec < 4 || nvec > 128) return GGRN_ERR_UNSUPPORTED;
+  const int lanes = next_pow2(static_cast<int>(ceil_div(nvec, 4)));
+  const int64_t tpw = 32 / lanes;
+  const int64_t gpr = a.width / a.gs;
+  const int64_t total = a.rows * gpr;
+  const bool flat = a.rows <= 1 || (a.ys == a.width && a.gts == a.width && a.os == a.width);
+  int W = 0, mode = 0;
+  int64_t ug = 0, units = 0, upr = 0, rpu = 0;
+  if (flat) {
+    // consecutive groups of the contiguous [rows * width] data
+    mode = 0;
+    W = kStreamWarps;
+    ug = W * tpw;
+    units = ceil_div(total, ug);
+    const int64_t last = total - (units - 1) * ug;
+    if ((ug * gbytes) % 16 != 0 || (last * gbytes) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
+  } else {
+    // units inside a row: ug = W * tpw must divide the row's groups
+    for (int w = 4; w <= 16; ++w) {
+      const int64_t u = w * tpw;
+      if (gpr % u != 0 || (u * gbytes) % 16 != 0) continue;
+      if (W == 0 || std::abs(w - kStreamWarps) <= std::abs(W - kStreamWarps)) W = w;
+    }
+    if (W != 0) {
+      mode = 1;
+      ug = W * tpw;
+      upr = gpr / ug;
+      units = a.rows * upr;
+    } else {
+      // short rows: whole rows per unit, each row copied on its own
+      if ((a.width * es) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
+      mode = 2;
+      rpu = std::max<int64_t>(1, (kStreamWarps * tpw) / gpr);
+      W = static_cast<int>(ceil_div(rpu * gpr, tpw));
+      if (W > 16) return GGRN_ERR_UNSUPPORTED;
+      ug = rpu * gpr;
+      units = ceil_div(a.rows, rpu);
+    }
+  }
+  const uint32_t stage_bytes = static_cast<uint32_t>(ceil_div(ug * gbytes, 128) * 128);
+  // The weight is staged in shared memory once per CTA when its bytes are a
+  // 16-byte multiple and it leaves room for the ring.
+  const int64_t wb = a.mode == kMamba2 ? a.width * 4 : a.gs * es;
+  int cps = 0, ns = 0;
+  int64_t wstage = 0;
+  for (int staged = 1; staged >= 0 && ns < 2; --staged) {
+    const int64_t warea = staged ? ceil_div(wb, 128) * 128 : 0;
+    if (staged && (wb % 16 != 0 || wb > kStreamMaxWeightBytes)) continue;
+    for (int c = 2; c >= 1; --c) {
+      const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 256;
+      const int64_t n = std::min<int64_t>(kStreamMaxStages, budget / (2 * stage_bytes));
+      if (n >= 2) {
+        cps = c;
+        ns = static_cast<int>(n);
+        wstage = staged ? wb : 0;
+        break;
+      }
+    }
+  }
+  if (ns < 2) return GGRN_ERR_UNSUPPORTED;
+  const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
+  if (!forced && units < 2 * gmax) return GGRN_ERR_UNSUPPORTED;
+  // equal units per CTA: the last wave ends together
+  const int64_t per_cta = ceil_div(units, gmax);
+  p->path = kStream;
+  p->elems_per_vec = se;
+  p->smem_vec_bytes = sv;
+  p->nvec = static_cast<int>(nvec);
+  p->vpl = 4;
+  p->lanes = lanes;
+  p->consumer_warps = W;
+  p->ug = static_cast<int>(ug);
+  p->units_per_row = upr;
+  p->unit_mode = mode;
+  p->rows_per_unit = static_cast<int>(rpu);
+  p->total_groups = total;
+  p->groups = gpr;
+  p->items = units;
+  p->stage_bytes = stage_bytes;
+  p->stages = ns;
+  p->ctas_per_sm = cps;
+  p->grid = ceil_div(units, per_cta);
+  p->block = (W + 1) * 32;
+  p->w_smem_bytes = static_cast<uint32_t>(wstage);
+  p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes +
+                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 1));
+  p->div_magic = mode == 1 ? div_magic(units, upr) : 0;
+  p->div_magic2 = div_magic(total, gpr);
+  return GGRN_OK;
+}
+
 int make_plan(const Args& a, int path, Plan* p) {
   *p = Plan();
   const bool vec_ok = vector_layout_ok(a);
   switch (path) {
     case kAuto: {
       if (vec_ok) {
+        // streaming with 16-byte shared-memory vectors; odd spans measured
+        // faster on the register-resident straddle family
+        if (plan_stream(a, p, false) == GGRN_OK && p->smem_vec_bytes == 16) return GGRN_OK;
+        *p = Plan();
         if (plan_team(a, p) == GGRN_OK) return GGRN_OK;
         if (plan_wide(a, p) == GGRN_OK) return GGRN_OK;
         if (plan_straddle(a, p) == GGRN_OK) return GGRN_OK;
@@ -285,6 +421,9 @@ int make_plan(const Args& a, int path, Plan* p) {
       return plan_straddle(a, p);
     case kScalar:
       return plan_scalar(a, p);
+    case kStream:
+      if (!vec_ok) return GGRN_ERR_ALIGN;
+      return plan_stream(a, p, true);
     default:
       return GGRN_ERR_ARG;
   }
@@ -313,14 +452,22 @@ Args make_args(const void* y, const void* gate, const void* w, void* out, int64_
 
 int launch(const Args& a, const Plan& p, cudaStream_t s) {
   if (p.grid == 0) return GGRN_OK;
-  const KParams k = make_params(a, p);
+  KParams k = make_params(a, p);
+  if (p.path == kStream) {
+    k.fault = fault_word();
+    if (!k.fault) return GGRN_ERR_CUDA;
+  }
   cudaError_t e;
   switch (a.dtype) {
     case kF32: e = launch_f32(k, p, a.mode, s); break;
     case kF16: e = launch_f16(k, p, a.mode, s); break;
     default: e = launch_bf16(k, p, a.mode, s); break;
   }
-  return e == cudaSuccess ? GGRN_OK : GGRN_ERR_CUDA;
+  if (e != cudaSuccess) {
+    tl_last_cuda_error = e;
+    return GGRN_ERR_CUDA;
+  }
+  return GGRN_OK;
 }
 
 int forward_impl(const Args& a, int path, cudaStream_t s) {
@@ -358,6 +505,19 @@ KParams make_params(const Args& a, const Plan& p) {
   k.warp_smem = p.warp_smem;
   k.gs_magic = p.gs_magic;
   k.div_magic = p.div_magic;
+  k.div_magic2 = p.div_magic2;
+  k.units = p.items;
+  k.units_per_row = p.units_per_row;
+  k.total_groups = p.total_groups;
+  k.consumer_warps = p.consumer_warps;
+  k.stages = p.stages;
+  k.stage_bytes = p.stage_bytes;
+  k.w_smem_bytes = p.w_smem_bytes;
+  k.ug = p.ug;
+  k.unit_mode = p.unit_mode;
+  k.rows_per_unit = p.rows_per_unit;
+  k.rows = a.rows;
+  k.fault = nullptr;
   k.eps = a.eps;
   k.gs_f = static_cast<float>(a.gs);
   return k;
@@ -382,7 +542,7 @@ extern "C" int ggrn_forward_path(const void* y, const void* gate, const void* w,
                                  int64_t y_row_stride, int64_t gate_row_stride,
                                  int64_t out_row_stride, float eps, int dtype, int mode,
                                  int path, void* cuda_stream) {
-  if (path < kAuto || path > kScalar) return GGRN_ERR_ARG;
+  if (path < kAuto || path > kStream) return GGRN_ERR_ARG;
   const Args a = make_args(y, gate, w, out, rows, width, group_size, y_row_stride,
                            gate_row_stride, out_row_stride, eps, dtype, mode);
   return forward_impl(a, path, static_cast<cudaStream_t>(cuda_stream));
@@ -393,7 +553,7 @@ extern "C" int ggrn_plan(const void* y, const void* gate, const void* w, const v
                          int64_t gate_row_stride, int64_t out_row_stride, int dtype, int mode,
                          int path, ggrn_plan_info* info) {
   if (!info) return GGRN_ERR_ARG;
-  if (path < kAuto || path > kScalar) return GGRN_ERR_ARG;
+  if (path < kAuto || path > kStream) return GGRN_ERR_ARG;
   std::memset(info, 0, sizeof(*info));
   const Args a = make_args(y, gate, w, const_cast<void*>(out), rows, width, group_size,
                            y_row_stride, gate_row_stride, out_row_stride, 0.0f, dtype, mode);
@@ -427,6 +587,7 @@ extern "C" int ggrn_graph_create(const ggrn_call* calls, int32_t n, void** graph
     Plan p;
     if (a.rows > 0 && (st = make_plan(a, kAuto, &p)) != GGRN_OK) return st;
   }
+  if (!fault_word()) return GGRN_ERR_CUDA;  // symbol lookup before the capture starts
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GGRN_ERR_CUDA;
   int status = GGRN_OK;
@@ -492,3 +653,21 @@ extern "C" const char* ggrn_status_string(int status) {
 }
 
 extern "C" int ggrn_version(void) { return 100; }
+
+extern "C" int ggrn_fault_status(uint32_t* flags, int clear) {
+  if (!flags) return GGRN_ERR_ARG;
+  *flags = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GGRN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_ggrn_fault, sizeof(v)) != cudaSuccess) return GGRN_ERR_CUDA;
+  *flags = v;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_ggrn_fault, &zero, sizeof(zero)) != cudaSuccess) return GGRN_ERR_CUDA;
+  }
+  return GGRN_OK;
+}
+
+extern "C" const char* ggrn_last_cuda_error(void) {
+  return cudaGetErrorName(tl_last_cuda_error);
+}

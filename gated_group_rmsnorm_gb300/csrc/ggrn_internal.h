@@ -9,7 +9,7 @@ namespace ggrn {
 
 enum Mode : int { kMamba2 = 0, kOnnx = 1 };
 enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
-enum Path : int { kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4 };
+enum Path : int { kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4, kStream = 5 };
 
 // Validated arguments of one call.
 struct Args {
@@ -26,13 +26,13 @@ struct Args {
 // A launch decision.
 struct Plan {
   int path = kAuto;
-  int lanes = 0;        // TEAM: lanes per group (1..32)
-  int vpl = 0;          // 16-byte vectors per lane per tensor
+  int lanes = 0;        // TEAM/STREAM: lanes per group (1..32)
+  int vpl = 0;          // vectors per lane per tensor
   int elems_per_vec = 1;
   int block = 0;        // threads per CTA
   int smem = 0;         // dynamic shared memory bytes
   int64_t grid = 0;     // CTAs
-  int64_t items = 0;    // groups, or row chunks (STRADDLE)
+  int64_t items = 0;    // groups, row chunks (STRADDLE) or units (STREAM)
   int64_t groups = 0;   // groups per row
   int nvec = 0;         // TEAM/WIDE: vectors per group; STRADDLE: vectors per chunk (max)
   // STRADDLE
@@ -43,6 +43,19 @@ struct Plan {
   uint32_t gs_magic = 0;       // floor(2^32 / gs) + 1: exact floor(x / gs) for x, gs < 2^11
   int warp_smem = 0;           // floats of shared memory per warp
   uint64_t div_magic = 0;      // floor(2^64 / items_per_row) + 1, or 0 (see div_by)
+  // STREAM
+  int smem_vec_bytes = 0;      // 16 or 8
+  int consumer_warps = 0;
+  int stages = 0;
+  uint32_t stage_bytes = 0;    // one tensor's chunk slot, 128-byte aligned
+  uint32_t w_smem_bytes = 0;   // weight staged in shared memory (0: read from global)
+  int ug = 0;                  // groups per unit
+  int64_t units_per_row = 0;   // chunk units per row
+  int64_t total_groups = 0;
+  int unit_mode = 0;           // 0 flat (contiguous rows), 1 chunk of a row, 2 whole rows
+  int rows_per_unit = 0;       // unit_mode 2
+  uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
+  int ctas_per_sm = 0;
 };
 
 // Kernel parameters (passed by value).
@@ -51,6 +64,7 @@ struct KParams {
   const void* gate;
   const void* w;
   void* out;
+  unsigned int* fault;     // device status word (bits of ggrn_fault_status)
   int64_t items;
   int64_t groups;          // groups per row
   int64_t width;
@@ -58,11 +72,23 @@ struct KParams {
   int64_t ys, gts, os;
   int64_t chunk_elems;
   int64_t chunks_per_row;
+  int64_t units;
+  int64_t units_per_row;
+  int64_t total_groups;
+  uint64_t div_magic;
+  uint64_t div_magic2;
   int nvec;
   int chunk_groups;
   int warp_smem;
   uint32_t gs_magic;
-  uint64_t div_magic;
+  int consumer_warps;
+  int stages;
+  uint32_t stage_bytes;
+  uint32_t w_smem_bytes;
+  int ug;
+  int unit_mode;
+  int rows_per_unit;
+  int64_t rows;
   float eps;
   float gs_f;
 };

@@ -641,6 +641,10 @@ __global__ void __launch_bounds__(256) k_scalar(const KParams p) {
 // ---------------------------------------------------------------------------
 // Launch of the kernel a plan names, for one element type.
 // ---------------------------------------------------------------------------
+// The streaming family lives in ggrn_stream.cuh.
+template <typename T, int MODE>
+cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s);
+
 template <typename K>
 cudaError_t launch_kernel(K kernel, const KParams& k, const Plan& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -706,6 +710,8 @@ cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
       if (p.lanes == 1) return launch_kernel(k_scalar<T, MODE, 1>, k, p, s);
       if (p.lanes == 32) return launch_kernel(k_scalar<T, MODE, 32>, k, p, s);
       break;
+    case kStream:
+      return launch_stream<T, MODE>(k, p, s);
     default:
       break;
   }

@@ -1,5 +1,5 @@
 // fp16 instantiations of the fused gated group-RMSNorm kernels.
-#include "ggrn_kernels.cuh"
+#include "ggrn_stream.cuh"
 
 namespace ggrn {
 cudaError_t launch_f16(const KParams& k, const Plan& p, int mode, cudaStream_t s) {

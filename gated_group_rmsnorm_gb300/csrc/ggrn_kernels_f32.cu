@@ -1,5 +1,5 @@
 // f32 instantiations of the fused gated group-RMSNorm kernels.
-#include "ggrn_kernels.cuh"
+#include "ggrn_stream.cuh"
 
 namespace ggrn {
 cudaError_t launch_f32(const KParams& k, const Plan& p, int mode, cudaStream_t s) {

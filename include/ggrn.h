@@ -75,12 +75,16 @@ typedef enum {
                              the team is narrower than a warp (narrow and medium groups) */
   GGRN_PATH_WIDE = 2,     /* one CTA per group, group held in registers across the CTA,
                              warp partials combined through shared memory (wide groups) */
-  GGRN_PATH_STRADDLE = 3, /* one CTA per row (or row chunk); 16-byte vectors that straddle
-                             group boundaries; per-vector partial sums combined per group
-                             through shared memory (group_size not a multiple of the vector) */
-  GGRN_PATH_SCALAR = 4    /* element loads, any alignment and any group size; the group is
+  GGRN_PATH_STRADDLE = 3, /* one warp per row chunk; 16-byte vectors that straddle group
+                             boundaries; per-vector partial sums combined per group through
+                             shared memory (group_size not a multiple of the vector) */
+  GGRN_PATH_SCALAR = 4,   /* element loads, any alignment and any group size; the group is
                              read twice (a correctness path for layouts the vector paths
                              cannot load) */
+  GGRN_PATH_STREAM = 5    /* persistent CTAs; a producer lane streams row chunks into a
+                             shared-memory ring with bulk (TMA) copies, consumer warps
+                             reduce from shared memory (group bytes a multiple of 8,
+                             4..128 shared-memory vectors per group, enough rows) */
 } ggrn_path;
 
 /*
@@ -176,6 +180,22 @@ const char* ggrn_status_string(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int ggrn_version(void);
+
+/*
+ * ggrn_fault_status -- the device status word of the current device.  The
+ * STREAM kernels bound every wait on a shared-memory barrier; a wait that
+ * runs out stops the kernel and sets a bit here: 1 = a consumer waited for
+ * data, 2 = the producer waited for a free stage, 4 = the producer waited for
+ * its copies to land.  Nonzero means the outputs of some call are
+ * incomplete.  Synchronises the device, writes the word to *flags and, when
+ * `clear` is nonzero, resets it.  Returns GGRN_OK, GGRN_ERR_ARG (flags NULL)
+ * or GGRN_ERR_CUDA.
+ */
+int ggrn_fault_status(uint32_t* flags, int clear);
+
+/* Name of the CUDA error behind this thread's last GGRN_ERR_CUDA from a
+ * launch ("cudaSuccess" if none); a static string, never NULL. */
+const char* ggrn_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -108,21 +108,36 @@ def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
 
 
 def test_plan_selects_families():
-    # Mamba-2 prefill 4096x7680, group 960 (120 vectors): one warp per group, 4 vectors/lane
+    # Mamba-2 prefill 4096x7680, group 960: streamed, one row (8 groups) per
+    # unit, one warp per group (32 lanes x 4 vectors of 16 bytes), 8 consumer
+    # warps + 1 producer warp, 14 units per CTA on 152 SMs x 2 CTAs
     p = _plan(4096, 7680, 960, 2)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads) == \
+        (g.PATH_STREAM, 32, 4, 4096, 288)
+    assert p.grid_blocks == -(-4096 // 14)
+    # the same shape on the register-resident family: one warp per group
+    p = _plan(4096, 7680, 960, 2, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
     # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 4-lane teams with 4
-    # vectors each, 8 groups per warp
+    # vectors each, 8 groups per warp; streamed in units of 64 groups (2 rows)
     p = _plan(32768, 4096, 128, 1, mode=1)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_STREAM, 4, 4, 16384)
+    p = _plan(32768, 4096, 128, 1, mode=1, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 4)
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
-    # odd span 100 at row stride 9664: straddling vectors; one warp per chunk
-    # of 5 periods (lcm(100, 8) = 200 elements = 25 vectors) in 128 slots,
-    # 5 chunks per row
+    # odd span 100 (200 bytes) at row stride 9664: the register-resident
+    # straddle family, one warp per chunk of 5 periods (lcm(100, 8) = 200
+    # elements = 25 vectors) in 128 slots, 5 chunks per row
     p = _plan(65536, 4800, 100, 2, ys=9664)
     assert (p.path, p.block_threads, p.vec_per_lane, p.items) == (g.PATH_STRADDLE, 256, 4, 5 * 65536)
+    # forced onto the streaming family: 8-byte shared-memory vectors (25 per
+    # group, 8 lanes x 4); units of 24 groups inside a row (6 consumer warps
+    # x 4 teams), 2 units per 48-group row
+    p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STREAM)
+    assert (p.path, p.team_lanes, p.elems_per_vec, p.items, p.block_threads) == \
+        (g.PATH_STREAM, 8, 4, 2 * 65536, 7 * 32)
     # a width that is not a multiple of the vector goes to the scalar path
     assert _plan(4, 300, 100, 2).path == g.PATH_SCALAR
     # decode (one row, 8 groups): one warp per CTA spreads the groups over SMs

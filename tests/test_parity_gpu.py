@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 MAMBA2, ONNX = 0, 1
 WL = ggrn_inputs.WORKLOADS
-PATHS = (g.PATH_AUTO, g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR)
+PATHS = (g.PATH_AUTO, g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR, g.PATH_STREAM)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -252,3 +252,51 @@ def test_deterministic_bits():
         b = _run(dev, wl)
         torch.cuda.synchronize()
         assert ulp_dist(a.cpu(), b.cpu()).max() == 0
+
+
+# Row counts for the streaming family: several units per CTA on some CTAs, a
+# ragged last wave, and (flat layouts) a partial last unit.
+STREAM_ROWS = {"mamba2_prefill": 1031, "gdn_onnx": 1023, "strided_odd_span": 777}
+
+
+@pytest.mark.parametrize("name", sorted(STREAM_ROWS))
+def test_stream_family(name):
+    """The bulk-copy streaming family, forced, against the oracle; and the
+    device status word stays clear (no bounded wait ran out)."""
+    g.fault_status(clear=True)
+    wl = WL[name].with_rows(STREAM_ROWS[name])
+    host = ggrn_inputs.make_inputs(wl)
+    dev = gpu_util.to_device(host)
+    assert g.plan(dev.y, dev.gate, dev.w, group_size=wl.group_size,
+                  mode=wl.mode, path=g.PATH_STREAM)["path"] == g.PATH_STREAM
+    out = _run(dev, wl, path=g.PATH_STREAM)
+    out2 = _run(dev, wl, path=g.PATH_STREAM)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    res = gpu_util.compare(out, host, wl.group_size, wl.eps, wl.mode)
+    assert res["ok"], res
+    assert g.fault_status() == 0
+
+
+def test_stream_flat_partial_unit_and_strided_out():
+    """Flat rows whose group count leaves a partial last unit; then the same
+    data with a strided output (units stay inside a row)."""
+    for dtype, mode, gs in ((torch.bfloat16, MAMBA2, 64), (torch.float16, ONNX, 256),
+                            (torch.float32, MAMBA2, 128), (torch.bfloat16, MAMBA2, 100)):
+        rows, width = 613, gs * 6
+        inp = ggrn_inputs.random_case(rows, width, gs, dtype, mode, 31)
+        dev = gpu_util.to_device(inp)
+        out = g.forward(dev.y, dev.gate, dev.w, group_size=gs, eps=1e-5, mode=mode,
+                        path=g.PATH_STREAM)
+        torch.cuda.synchronize()
+        res = gpu_util.compare(out, inp, gs, 1e-5, mode)
+        assert res["ok"], (dtype, gs, res)
+        big = torch.zeros(rows, width + 64, dtype=dtype, device="cuda")
+        ov = big[:, 32:32 + width]
+        g.forward(dev.y, dev.gate, dev.w, group_size=gs, eps=1e-5, mode=mode, out=ov,
+                  path=g.PATH_STREAM)
+        torch.cuda.synchronize()
+        assert torch.equal(ov.cpu().view(torch.int16) if dtype != torch.float32 else ov.cpu(),
+                           out.cpu().view(torch.int16) if dtype != torch.float32 else out.cpu())
+        assert bool((big[:, :32] == 0).all()) and bool((big[:, 32 + width:] == 0).all())
+    assert g.fault_status() == 0
