@@ -293,21 +293,32 @@ int plan_scalar(const Args& a, Plan* p) {
 }
 
 // STREAM: persistent CTAs fed by bulk copies of row chunks ("units" of ug
-// whole groups).  Eligible when a group's bytes are a multiple of 8, it
-// spans 4..128 shared-memory vectors, every unit is a 16-byte multiple, and
-// there are at least two units per CTA slot.
+// whole groups).  A team takes an item of Q groups: Q = 1 when a group's
+// bytes are a multiple of 16 (or of 8, with 8-byte shared-memory vectors),
+// Q = 2 when they are an odd multiple of 8 (a pair of groups is then whole
+// 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
+// vectors, every unit is a 16-byte multiple, and (unless forced) there are
+// at least two units per CTA slot.
 int plan_stream(const Args& a, Plan* p, bool forced) {
   const int es = elem_size(a.dtype);
   const int64_t gbytes = a.gs * es;
-  const int sv = (gbytes % 16 == 0) ? 16 : (gbytes % 8 == 0 ? 8 : 0);
-  if (sv == 0) return GGRN_ERR_UNSUPPORTED;
+  int sv = 0, Q = 1;
+  if (gbytes % 16 == 0) {
+    sv = 16;
+  } else if (gbytes % 8 == 0) {
+    sv = 16;
+    Q = 2;
+  } else {
+    return GGRN_ERR_UNSUPPORTED;
+  }
   const int se = sv / es;
-  const int64_t nvec = a.gs / se;
+  const int64_t nvec = Q * a.gs / se;     // vectors per item
   if (nvec < 4 || nvec > 128) return GGRN_ERR_UNSUPPORTED;
   const int lanes = next_pow2(static_cast<int>(ceil_div(nvec, 4)));
-  const int64_t tpw = 32 / lanes;
+  const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass
   const int64_t gpr = a.width / a.gs;
   const int64_t total = a.rows * gpr;
+  if (gpr % Q != 0) return GGRN_ERR_UNSUPPORTED;  // items never cross a row
   const bool flat = a.rows <= 1 || (a.ys == a.width && a.gts == a.width && a.os == a.width);
   int W = 0, mode = 0;
   int64_t ug = 0, units = 0, upr = 0, rpu = 0;
@@ -315,28 +326,28 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
     // consecutive groups of the contiguous [rows * width] data
     mode = 0;
     W = kStreamWarps;
-    ug = W * tpw;
+    ug = W * gpw;
     units = ceil_div(total, ug);
     const int64_t last = total - (units - 1) * ug;
     if ((ug * gbytes) % 16 != 0 || (last * gbytes) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
   } else {
-    // units inside a row: ug = W * tpw must divide the row's groups
+    // units inside a row: ug = W * gpw must divide the row's groups
     for (int w = 4; w <= 16; ++w) {
-      const int64_t u = w * tpw;
+      const int64_t u = w * gpw;
       if (gpr % u != 0 || (u * gbytes) % 16 != 0) continue;
       if (W == 0 || std::abs(w - kStreamWarps) <= std::abs(W - kStreamWarps)) W = w;
     }
     if (W != 0) {
       mode = 1;
-      ug = W * tpw;
+      ug = W * gpw;
       upr = gpr / ug;
       units = a.rows * upr;
     } else {
       // short rows: whole rows per unit, each row copied on its own
       if ((a.width * es) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
       mode = 2;
-      rpu = std::max<int64_t>(1, (kStreamWarps * tpw) / gpr);
-      W = static_cast<int>(ceil_div(rpu * gpr, tpw));
+      rpu = std::max<int64_t>(1, (kStreamWarps * gpw) / gpr);
+      W = static_cast<int>(ceil_div(rpu * gpr, gpw));
       if (W > 16) return GGRN_ERR_UNSUPPORTED;
       ug = rpu * gpr;
       units = ceil_div(a.rows, rpu);
@@ -370,6 +381,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->path = kStream;
   p->elems_per_vec = se;
   p->smem_vec_bytes = sv;
+  p->items_groups = Q;
   p->nvec = static_cast<int>(nvec);
   p->vpl = 4;
   p->lanes = lanes;
@@ -400,9 +412,11 @@ int make_plan(const Args& a, int path, Plan* p) {
   switch (path) {
     case kAuto: {
       if (vec_ok) {
-        // streaming with 16-byte shared-memory vectors; odd spans measured
-        // faster on the register-resident straddle family
-        if (plan_stream(a, p, false) == GGRN_OK && p->smem_vec_bytes == 16) return GGRN_OK;
+        // streaming for groups of whole 16-byte vectors; odd spans (paired
+        // items leave a quarter of the lane slots idle) measured faster on
+        // the register-resident straddle family
+        if (plan_stream(a, p, false) == GGRN_OK && p->smem_vec_bytes == 16 && p->items_groups == 1)
+          return GGRN_OK;
         *p = Plan();
         if (plan_team(a, p) == GGRN_OK) return GGRN_OK;
         if (plan_wide(a, p) == GGRN_OK) return GGRN_OK;

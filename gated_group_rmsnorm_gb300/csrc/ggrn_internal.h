@@ -45,6 +45,7 @@ struct Plan {
   uint64_t div_magic = 0;      // floor(2^64 / items_per_row) + 1, or 0 (see div_by)
   // STREAM
   int smem_vec_bytes = 0;      // 16 or 8
+  int items_groups = 1;        // groups per team item (2: pairs of odd-half-vector groups)
   int consumer_warps = 0;
   int stages = 0;
   uint32_t stage_bytes = 0;    // one tensor's chunk slot, 128-byte aligned

@@ -159,15 +159,16 @@ __device__ __forceinline__ void round_to_t(float* f) {
 
 // ---------------------------------------------------------------------------
 // k_stream: TEAM consumers.  SV = bytes per shared-memory vector (16 or 8),
-// SE = elements per vector, L lanes per group, VPL vectors per lane.
+// SE = elements per vector, L lanes per team, VPL vectors per lane, Q groups
+// per team item (1, or 2 for groups of an odd number of half vectors).
 // Dynamic shared memory: [stages][y chunk | gate chunk] then the barriers.
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, int L, int VPL, int SV>
+template <typename T, int MODE, int L, int VPL, int SV, int Q>
 __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
   constexpr int ES = sizeof(T);
   constexpr int SE = SV / ES;
   constexpr int NW = SV / 4;
-  constexpr int TPW = 32 / L;  // teams (groups) per warp
+  constexpr int TPW = 32 / L;  // teams (items) per warp
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int W = p.consumer_warps;
@@ -262,10 +263,15 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
   }
 
   // ---------------- consumers ----------------
+  // A team takes an "item" of Q consecutive groups.  Q = 2 pairs groups whose
+  // bytes are an odd multiple of half a vector: the pair is whole 16-byte
+  // vectors, and the one vector across the boundary (vector vb) splits at its
+  // middle, its low half ending the first group.
   const int team = lane / L;
   const int tl = lane & (L - 1);
-  const int nvec = static_cast<int>(gs / SE);
-  const int groups_per_pass = W * TPW;
+  const int nvec = static_cast<int>(Q * gs / SE);
+  const int vb = static_cast<int>(gs / SE);
+  const int items_per_pass = W * TPW;
   int64_t i = 0;
   for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
     const int s = static_cast<int>(i % NS);
@@ -286,12 +292,14 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
       row_u = u * p.rows_per_unit;
       ngroups = min(static_cast<int64_t>(p.rows_per_unit), p.rows - row_u) * p.groups;
     }
+    const int nitems = static_cast<int>(ngroups / Q);
     const unsigned char* sy = smem + static_cast<size_t>(2) * s * sb;
     const unsigned char* sg = sy + sb;
-    for (int pass = 0; pass * groups_per_pass < ngroups; ++pass) {
-      const int gl = pass * groups_per_pass + warp * TPW + team;  // group within the unit
-      const bool active = gl < ngroups;
-      // output origin and weight column of this group
+    for (int pass = 0; pass * items_per_pass < nitems; ++pass) {
+      const int item = pass * items_per_pass + warp * TPW + team;
+      const bool active = item < nitems;
+      const int gl = item * Q;  // first group of the item within the unit
+      // output origin and weight column of that group
       int64_t out_off, wcol;
       if (p.unit_mode == kUnitFlat) {
         const int64_t G = g0 + gl;
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
         }
       }
       float a[VPL][SE];
-      float ss = 0.0f;
+      float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
         float yf[SE];
@@ -336,18 +344,36 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
 #pragma unroll
           for (int e = 0; e < SE; ++e) a[k][e] = yf[e];
         }
+        if constexpr (Q == 1) {
 #pragma unroll
-        for (int e = 0; e < SE; ++e) ss = fmaf(a[k][e], a[k][e], ss);
+          for (int e = 0; e < SE; ++e) s0 = fmaf(a[k][e], a[k][e], s0);
+        } else {
+          float h0 = 0.0f, h1 = 0.0f;
+#pragma unroll
+          for (int e = 0; e < SE / 2; ++e) h0 = fmaf(a[k][e], a[k][e], h0);
+#pragma unroll
+          for (int e = SE / 2; e < SE; ++e) h1 = fmaf(a[k][e], a[k][e], h1);
+          const int v = k * L + tl;
+          s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
+          s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
+        }
       }
 #pragma unroll
-      for (int o = L / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float nf = normaliser(ss, p.gs_f, p.eps);
+      for (int o = L / 2; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        if constexpr (Q == 2) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      const float nf0 = normaliser(s0, p.gs_f, p.eps);
+      const float nf1 = (Q == 2) ? normaliser(s1, p.gs_f, p.eps) : nf0;
 
       T* op = static_cast<T*>(p.out) + out_off;
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
         const int v = k * L + tl;
         if (active && v < nvec) {
+          // normaliser of each half of the vector
+          const float nlo = (Q == 1 || v <= vb) ? nf0 : nf1;
+          const float nhi = (Q == 1 || v < vb) ? nf0 : nf1;
           float r[SE];
           if (MODE == kMamba2) {
             float wv[SE];
@@ -368,18 +394,32 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
               }
             }
 #pragma unroll
-            for (int e = 0; e < SE; ++e) r[e] = a[k][e] * nf;
+            for (int e = 0; e < SE; ++e) r[e] = a[k][e] * (e < SE / 2 ? nlo : nhi);
             round_to_t<T, SE>(r);
 #pragma unroll
             for (int e = 0; e < SE; ++e) r[e] = wv[e] * r[e];
           } else {
             float sc[SE], gf[SE];
-            words_to_f32<T, NW>(wbytes ? lds_words<NW>(wsm + v * SV)
-                                       : ldg_words<NW>(static_cast<const T*>(p.w) + v * SE),
-                                sc);
+            if constexpr (Q == 1) {
+              words_to_f32<T, NW>(wbytes ? lds_words<NW>(wsm + v * SV)
+                                         : ldg_words<NW>(static_cast<const T*>(p.w) + v * SE),
+                                  sc);
+            } else {
+              // scale index restarts at each group: each half has its own offset
+              const int jlo = v * SE - (v <= vb ? 0 : static_cast<int>(gs));
+              const int jhi = v * SE + SE / 2 - (v < vb ? 0 : static_cast<int>(gs));
+              const T* wt = static_cast<const T*>(p.w);
+              words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jlo * ES)
+                                             : ldg_words<NW / 2>(wt + jlo),
+                                      sc);
+              words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jhi * ES)
+                                             : ldg_words<NW / 2>(wt + jhi),
+                                      sc + SE / 2);
+            }
             words_to_f32<T, NW>(gr[k], gf);
 #pragma unroll
-            for (int e = 0; e < SE; ++e) r[e] = ((a[k][e] * nf) * sc[e]) * silu<T>(gf[e]);
+            for (int e = 0; e < SE; ++e)
+              r[e] = ((a[k][e] * (e < SE / 2 ? nlo : nhi)) * sc[e]) * silu<T>(gf[e]);
           }
           stg_words<NW>(op + v * SE, f32_to_words<T, NW>(r));
         }
@@ -413,15 +453,15 @@ cudaError_t launch_stream_kernel(const KParams& k, const Plan& p, cudaStream_t s
   return launch_kernel(kernel, k, p, s);
 }
 
-template <typename T, int MODE, int SV>
+template <typename T, int MODE, int SV, int Q>
 cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
   switch (p.lanes) {
-    case 1: return launch_stream_kernel<k_stream<T, MODE, 1, 4, SV>>(k, p, s);
-    case 2: return launch_stream_kernel<k_stream<T, MODE, 2, 4, SV>>(k, p, s);
-    case 4: return launch_stream_kernel<k_stream<T, MODE, 4, 4, SV>>(k, p, s);
-    case 8: return launch_stream_kernel<k_stream<T, MODE, 8, 4, SV>>(k, p, s);
-    case 16: return launch_stream_kernel<k_stream<T, MODE, 16, 4, SV>>(k, p, s);
-    case 32: return launch_stream_kernel<k_stream<T, MODE, 32, 4, SV>>(k, p, s);
+    case 1: return launch_stream_kernel<k_stream<T, MODE, 1, 4, SV, Q>>(k, p, s);
+    case 2: return launch_stream_kernel<k_stream<T, MODE, 2, 4, SV, Q>>(k, p, s);
+    case 4: return launch_stream_kernel<k_stream<T, MODE, 4, 4, SV, Q>>(k, p, s);
+    case 8: return launch_stream_kernel<k_stream<T, MODE, 8, 4, SV, Q>>(k, p, s);
+    case 16: return launch_stream_kernel<k_stream<T, MODE, 16, 4, SV, Q>>(k, p, s);
+    case 32: return launch_stream_kernel<k_stream<T, MODE, 32, 4, SV, Q>>(k, p, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -429,8 +469,9 @@ cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s) {
   if (p.vpl != 4) return cudaErrorInvalidConfiguration;
-  if (p.smem_vec_bytes == 16) return launch_stream_sv<T, MODE, 16>(k, p, s);
-  if (p.smem_vec_bytes == 8) return launch_stream_sv<T, MODE, 8>(k, p, s);
+  if (p.smem_vec_bytes == 16 && p.items_groups == 1) return launch_stream_sv<T, MODE, 16, 1>(k, p, s);
+  if (p.smem_vec_bytes == 16 && p.items_groups == 2) return launch_stream_sv<T, MODE, 16, 2>(k, p, s);
+  if (p.smem_vec_bytes == 8 && p.items_groups == 1) return launch_stream_sv<T, MODE, 8, 1>(k, p, s);
   return cudaErrorInvalidConfiguration;
 }
 

@@ -127,17 +127,22 @@ def test_plan_selects_families():
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
-    # odd span 100 (200 bytes) at row stride 9664: the register-resident
-    # straddle family, one warp per chunk of 5 periods (lcm(100, 8) = 200
-    # elements = 25 vectors) in 128 slots, 5 chunks per row
+    # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
+    # 9664: the register-resident straddle family, one warp per chunk of 5
+    # periods (lcm(100, 8) = 200 elements = 25 vectors) in 128 slots, 5
+    # chunks per row
     p = _plan(65536, 4800, 100, 2, ys=9664)
     assert (p.path, p.block_threads, p.vec_per_lane, p.items) == (g.PATH_STRADDLE, 256, 4, 5 * 65536)
-    # forced onto the streaming family: 8-byte shared-memory vectors (25 per
-    # group, 8 lanes x 4); units of 24 groups inside a row (6 consumer warps
-    # x 4 teams), 2 units per 48-group row
+    # forced onto the streaming family: paired groups, 25 16-byte vectors per
+    # pair (8 lanes x 4), one 48-group row per unit (6 consumer warps x 4
+    # teams x 2 groups)
     p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STREAM)
     assert (p.path, p.team_lanes, p.elems_per_vec, p.items, p.block_threads) == \
-        (g.PATH_STREAM, 8, 4, 2 * 65536, 7 * 32)
+        (g.PATH_STREAM, 8, 8, 65536, 7 * 32)
+    # a group of 12 bf16 (24 bytes): 8-byte shared-memory vectors are not
+    # chosen automatically; forced streaming pairs the groups (3 vectors per
+    # pair is below 4, so it is refused)
+    assert _plan(4096, 48 * 12, 12, 2).path != g.PATH_STREAM
     # a width that is not a multiple of the vector goes to the scalar path
     assert _plan(4, 300, 100, 2).path == g.PATH_SCALAR
     # decode (one row, 8 groups): one warp per CTA spreads the groups over SMs
