@@ -171,25 +171,33 @@ uint64_t div_magic(int64_t items, int64_t d) {
   return UINT64_MAX / static_cast<uint64_t>(d) + 1;
 }
 
-// One item per team or CTA; grid capped at the launch limit (the kernels
-// stride over the remaining items).
+// One item (a group, or a pair of groups) per team; grid capped at the
+// launch limit (the kernels stride over the remaining items).
 int plan_team(const Args& a, Plan* p) {
   const int es = elem_size(a.dtype);
   const int E = 16 / es;
-  if (a.gs % E != 0) return GGRN_ERR_UNSUPPORTED;
-  const int64_t nvec = a.gs / E;
-  if (nvec > kTeamMaxVec) return GGRN_ERR_UNSUPPORTED;
+  int Q = 1;
+  if (a.gs % E != 0) {
+    // groups of an odd number of half vectors go in pairs (whole vectors),
+    // when the row holds an even number of them
+    if ((2 * a.gs) % E != 0 || (a.width / a.gs) % 2 != 0) return GGRN_ERR_UNSUPPORTED;
+    Q = 2;
+  }
+  const int64_t nvec = Q * a.gs / E;
+  if (nvec > kTeamMaxVec || (Q == 2 && nvec < 4)) return GGRN_ERR_UNSUPPORTED;
   p->path = kTeam;
   p->elems_per_vec = E;
+  p->items_groups = Q;
   p->nvec = static_cast<int>(nvec);
   // Four vectors per lane (fewer for tiny groups) and as many lanes as that
-  // needs: the per-group costs (indexing, butterfly, normaliser) then spread
-  // over at least 32 elements per lane, and a warp serves 32/lanes groups.
+  // needs: the per-item costs (indexing, butterfly, normaliser) then spread
+  // over at least 32 elements per lane, and a warp serves 32/lanes items.
   p->vpl = nvec >= 4 ? 4 : next_pow2(static_cast<int>(nvec));
   p->lanes = next_pow2(static_cast<int>(ceil_div(nvec, p->vpl)));
   p->groups = a.width / a.gs;
-  p->items = a.rows * p->groups;
-  p->div_magic = div_magic(p->items, p->groups);
+  p->items_per_row = p->groups / Q;
+  p->items = a.rows * p->items_per_row;
+  p->div_magic = div_magic(p->items, p->items_per_row);
   // Spread small problems over the SMs: shrink the block (down to one warp)
   // while that keeps the grid under one CTA per SM.
   const int sms = sm_count();
@@ -507,6 +515,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.out = a.out;
   k.items = p.items;
   k.groups = p.groups;
+  k.items_per_row = p.items_per_row;
   k.width = a.width;
   k.gs = a.gs;
   k.ys = a.ys;

@@ -34,6 +34,7 @@ struct Plan {
   int64_t grid = 0;     // CTAs
   int64_t items = 0;    // groups, row chunks (STRADDLE) or units (STREAM)
   int64_t groups = 0;   // groups per row
+  int64_t items_per_row = 0;  // TEAM: items (groups or pairs of groups) per row
   int nvec = 0;         // TEAM/WIDE: vectors per group; STRADDLE: vectors per chunk (max)
   // STRADDLE
   int64_t chunk_elems = 0;     // elements per chunk (a multiple of lcm(gs, E))
@@ -68,6 +69,7 @@ struct KParams {
   unsigned int* fault;     // device status word (bits of ggrn_fault_status)
   int64_t items;
   int64_t groups;          // groups per row
+  int64_t items_per_row;   // TEAM: items per row
   int64_t width;
   int64_t gs;
   int64_t ys, gts, os;

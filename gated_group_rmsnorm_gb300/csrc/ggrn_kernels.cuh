@@ -265,14 +265,30 @@ __device__ __forceinline__ void load_weight_vec(const void* w, int64_t idx, floa
   }
 }
 
+// Half a vector (8 bytes) of the ONNX scale (T) at index j, widened.
+template <typename T>
+__device__ __forceinline__ void load_half_scale(const void* w, int64_t j, float* out) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const T*>(w) + j));
+  if constexpr (sizeof(T) == 4) {
+    out[0] = __uint_as_float(u.x);
+    out[1] = __uint_as_float(u.y);
+  } else {
+    Elem<T>::unpack2(u.x, out[0], out[1]);
+    Elem<T>::unpack2(u.y, out[2], out[3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
-// TEAM: LANES lanes per group, VPL 16-byte vectors per lane per tensor.
-// Vector v of a group (0 <= v < nvec) sits in slot k = v / LANES of lane
-// v % LANES, so each load instruction of a team covers LANES consecutive
-// vectors.  Teams are aligned LANES-lane segments of a warp; the xor
-// butterfly with offsets < LANES never crosses a segment.
+// TEAM: LANES lanes per item, VPL 16-byte vectors per lane per tensor.  An
+// item is Q consecutive groups: Q = 1, or Q = 2 for groups whose bytes are an
+// odd multiple of 8 (the pair is whole 16-byte vectors; the vector across
+// the boundary, vector vb, splits at its middle and two accumulators keep the
+// groups apart).  Vector v of an item (0 <= v < nvec) sits in slot
+// k = v / LANES of lane v % LANES, so each load instruction of a team covers
+// LANES consecutive vectors.  Teams are aligned LANES-lane segments of a
+// warp; the xor butterfly with offsets < LANES never crosses a segment.
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, int LANES, int VPL>
+template <typename T, int MODE, int LANES, int VPL, int Q>
 __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
   constexpr int E = Elem<T>::E;
   pdl_wait();
@@ -283,6 +299,7 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int team_in_warp = (threadIdx.x & 31) / LANES;
+  const int vb = static_cast<int>(p.gs / E);  // Q == 2: the vector split at its middle
 
   for (int64_t base = warp_id * teams_per_warp; base < p.items;
        base += warps_total * teams_per_warp) {
@@ -290,8 +307,8 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
     const bool active = item < p.items;
     int64_t row = 0, g = 0;
     if (active) {
-      row = div_by(item, p.groups, p.div_magic);
-      g = item - row * p.groups;
+      row = div_by(item, p.items_per_row, p.div_magic);
+      g = (item - row * p.items_per_row) * Q;  // first group of the item
     }
     const int64_t col0 = g * p.gs;
     const T* yp = static_cast<const T*>(p.y) + row * p.ys + col0;
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
     // MAMBA2: a = gated = y * silu(gate).  ONNX: a = x; the gate enters only
     // the epilogue, so its raw bits wait there and silu is evaluated once.
     float a[VPL][E];
-    float ss = 0.0f;
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
       float yf[E];
@@ -327,30 +344,64 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
 #pragma unroll
         for (int e = 0; e < E; ++e) a[k][e] = yf[e];
       }
+      if constexpr (Q == 1) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) ss = fmaf(a[k][e], a[k][e], ss);
+        for (int e = 0; e < E; ++e) s0 = fmaf(a[k][e], a[k][e], s0);
+      } else {
+        float h0 = 0.0f, h1 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) h0 = fmaf(a[k][e], a[k][e], h0);
+#pragma unroll
+        for (int e = E / 2; e < E; ++e) h1 = fmaf(a[k][e], a[k][e], h1);
+        const int v = k * LANES + lane;
+        s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
+        s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
+      }
     }
 #pragma unroll
-    for (int o = LANES / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float nf = normaliser(ss, p.gs_f, p.eps);
+    for (int o = LANES / 2; o > 0; o >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      if constexpr (Q == 2) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+    const float nf0 = normaliser(s0, p.gs_f, p.eps);
+    const float nf1 = (Q == 2) ? normaliser(s1, p.gs_f, p.eps) : nf0;
 
     T* op = static_cast<T*>(p.out) + row * p.os + col0;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
       const int v = k * LANES + lane;
       if (active && v < p.nvec) {
+        // normaliser of each half of the vector
+        const float nlo = (Q == 1 || v <= vb) ? nf0 : nf1;
+        const float nhi = (Q == 1 || v < vb) ? nf0 : nf1;
         float wv[E];
         uint4 o;
         if (MODE == kMamba2) {
           load_weight_vec<T, MODE>(p.w, col0 + (int64_t)v * E, wv);
-          o = epilogue_mamba2<T>(a[k], nf, wv);
+          float t[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) t[e] = a[k][e] * (e < E / 2 ? nlo : nhi);
+#pragma unroll
+          for (int e = 0; e < E; e += 2) Elem<T>::round_pair(t[e], t[e + 1]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) t[e] = wv[e] * t[e];
+          o = Elem<T>::pack(t);
         } else {
-          load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
-          float gf[E], sg[E];
+          if constexpr (Q == 1) {
+            load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
+          } else {
+            // the scale index restarts with each group: one offset per half
+            const int jlo = v * E - (v <= vb ? 0 : static_cast<int>(p.gs));
+            const int jhi = v * E + E / 2 - (v < vb ? 0 : static_cast<int>(p.gs));
+            load_half_scale<T>(p.w, jlo, wv);
+            load_half_scale<T>(p.w, jhi, wv + E / 2);
+          }
+          float gf[E], r[E];
           Elem<T>::unpack(gr[k], gf);
 #pragma unroll
-          for (int e = 0; e < E; ++e) sg[e] = silu<T>(gf[e]);
-          o = epilogue_onnx<T>(a[k], sg, nf, wv);
+          for (int e = 0; e < E; ++e)
+            r[e] = ((a[k][e] * (e < E / 2 ? nlo : nhi)) * wv[e]) * silu<T>(gf[e]);
+          o = Elem<T>::pack(r);
         }
         st_stream(op + (int64_t)v * E, o);
       }
@@ -688,15 +739,27 @@ template <typename T, int MODE>
 cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
   switch (p.path) {
     case kTeam:
+      if (p.items_groups == 2) {
+        switch (p.lanes * 8 + p.vpl) {   // paired items: at least 4 vectors
+          case 1 * 8 + 4: return launch_kernel(k_team<T, MODE, 1, 4, 2>, k, p, s);
+          case 2 * 8 + 4: return launch_kernel(k_team<T, MODE, 2, 4, 2>, k, p, s);
+          case 4 * 8 + 4: return launch_kernel(k_team<T, MODE, 4, 4, 2>, k, p, s);
+          case 8 * 8 + 4: return launch_kernel(k_team<T, MODE, 8, 4, 2>, k, p, s);
+          case 16 * 8 + 4: return launch_kernel(k_team<T, MODE, 16, 4, 2>, k, p, s);
+          case 32 * 8 + 4: return launch_kernel(k_team<T, MODE, 32, 4, 2>, k, p, s);
+          default: break;
+        }
+        break;
+      }
       switch (p.lanes * 8 + p.vpl) {   // (lanes, vectors per lane) pairs the host plans
-        case 1 * 8 + 1: return launch_kernel(k_team<T, MODE, 1, 1>, k, p, s);
-        case 1 * 8 + 2: return launch_kernel(k_team<T, MODE, 1, 2>, k, p, s);
-        case 1 * 8 + 4: return launch_kernel(k_team<T, MODE, 1, 4>, k, p, s);
-        case 2 * 8 + 4: return launch_kernel(k_team<T, MODE, 2, 4>, k, p, s);
-        case 4 * 8 + 4: return launch_kernel(k_team<T, MODE, 4, 4>, k, p, s);
-        case 8 * 8 + 4: return launch_kernel(k_team<T, MODE, 8, 4>, k, p, s);
-        case 16 * 8 + 4: return launch_kernel(k_team<T, MODE, 16, 4>, k, p, s);
-        case 32 * 8 + 4: return launch_kernel(k_team<T, MODE, 32, 4>, k, p, s);
+        case 1 * 8 + 1: return launch_kernel(k_team<T, MODE, 1, 1, 1>, k, p, s);
+        case 1 * 8 + 2: return launch_kernel(k_team<T, MODE, 1, 2, 1>, k, p, s);
+        case 1 * 8 + 4: return launch_kernel(k_team<T, MODE, 1, 4, 1>, k, p, s);
+        case 2 * 8 + 4: return launch_kernel(k_team<T, MODE, 2, 4, 1>, k, p, s);
+        case 4 * 8 + 4: return launch_kernel(k_team<T, MODE, 4, 4, 1>, k, p, s);
+        case 8 * 8 + 4: return launch_kernel(k_team<T, MODE, 8, 4, 1>, k, p, s);
+        case 16 * 8 + 4: return launch_kernel(k_team<T, MODE, 16, 4, 1>, k, p, s);
+        case 32 * 8 + 4: return launch_kernel(k_team<T, MODE, 32, 4, 1>, k, p, s);
         default: break;
       }
       break;

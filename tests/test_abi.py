@@ -128,10 +128,13 @@ def test_plan_selects_families():
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
-    # 9664: the register-resident straddle family, one warp per chunk of 5
-    # periods (lcm(100, 8) = 200 elements = 25 vectors) in 128 slots, 5
-    # chunks per row
+    # 9664: register-resident teams of 8 lanes x 4 vectors take pairs of
+    # groups (25 whole 16-byte vectors), 24 pairs per row
     p = _plan(65536, 4800, 100, 2, ys=9664)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 8, 4, 24 * 65536)
+    # the straddle family: one warp per chunk of 5 periods (lcm(100, 8) = 200
+    # elements = 25 vectors) in 128 slots, 5 chunks per row
+    p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STRADDLE)
     assert (p.path, p.block_threads, p.vec_per_lane, p.items) == (g.PATH_STRADDLE, 256, 4, 5 * 65536)
     # forced onto the streaming family: paired groups, 25 16-byte vectors per
     # pair (8 lanes x 4), one 48-group row per unit (6 consumer warps x 4
