@@ -471,6 +471,86 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_rows_sweep(args) -> None:
+    """Per-launch time against the row count of one workload, for the
+    automatic path and a forced family, with a CUDA-graph replay of the same
+    launches; a least-squares line time = fixed + per_row * rows separates
+    the fixed cost of a launch from its steady-state bandwidth.  One JSON
+    line per measurement, then one per fit."""
+    import gated_group_rmsnorm_gb300 as g
+    from gated_group_rmsnorm_gb300 import binding
+    torch.cuda.set_device(0)
+    L = g.load(build_if_missing=True)
+    base = ggrn_inputs.WORKLOADS[args.workload]
+    paths = [g.PATH_AUTO] + ([args.sweep_path] if args.sweep_path else [])
+    results = {}
+    for path in paths:
+        for rows in [int(r) for r in args.rows_sweep.split(",")]:
+            wl = base.with_rows(rows)
+            n_sets = max(2, -(-4 * L2_BYTES // wl.algorithmic_bytes()))
+            sets = [ggrn_inputs.make_inputs(wl, device="cuda", seed=s) for s in range(n_sets)]
+            outs = [torch.empty((rows, wl.width), dtype=wl.dtype, device="cuda") for _ in sets]
+            stream = torch.cuda.current_stream()
+            raw = [_raw_args(g, s, o, wl, ctypes.c_void_p(stream.cuda_stream)) for s, o in
+                   zip(sets, outs)]
+            for i in range(30):
+                a = raw[i % n_sets]
+                st = L.ggrn_forward_path(*a[:-1], path, a[-1])
+                if st != 0:
+                    raise RuntimeError(g.status_string(st))
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = args.steps
+            e0.record(stream)
+            for i in range(n):
+                a = raw[i % n_sets]
+                L.ggrn_forward_path(*a[:-1], path, a[-1])
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / n * 1e3
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            graph_calls = 20
+            with torch.cuda.stream(side):
+                raw_s = [a[:-1] + (ctypes.c_void_p(side.cuda_stream),) for a in raw]
+                with torch.cuda.graph(graph, stream=side):
+                    for i in range(graph_calls):
+                        a = raw_s[i % n_sets]
+                        L.ggrn_forward_path(*a[:-1], path, a[-1])
+            torch.cuda.synchronize()
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            reps = max(1, n // graph_calls)
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us_g = e0.elapsed_time(e1) / (reps * graph_calls) * 1e3
+            plan = g.plan(sets[0].y, sets[0].gate, sets[0].w, group_size=wl.group_size,
+                          mode=wl.mode, path=path)
+            line = {"workload": wl.name, "rows": rows, "path_requested": binding.PATH_NAMES[path],
+                    "path": plan["path_name"], "us_per_launch": round(us, 3),
+                    "us_per_launch_graph": round(us_g, 3),
+                    "gbs": round(wl.algorithmic_bytes() / us / 1e3, 1)}
+            print(json.dumps(line), flush=True)
+            results.setdefault(binding.PATH_NAMES[path], []).append((rows, us))
+            del sets, outs, graph
+            torch.cuda.empty_cache()
+    for name, pts in results.items():
+        n = len(pts)
+        mx = sum(r for r, _ in pts) / n
+        my = sum(t for _, t in pts) / n
+        b = sum((r - mx) * (t - my) for r, t in pts) / sum((r - mx) ** 2 for r, _ in pts)
+        a = my - b * mx
+        per_row_bytes = base.algorithmic_bytes() / base.rows
+        print(json.dumps({"fit": name, "workload": base.name, "fixed_us": round(a, 3),
+                          "per_row_ns": round(b * 1e3, 4),
+                          "steady_state_gbs": round(per_row_bytes / (b * 1e3), 1)}), flush=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,11 +566,20 @@ def main(argv=None) -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--rows-sweep", default="",
+                    help="comma-separated row counts: time per launch vs rows, and the fit "
+                         "(fixed cost, steady-state GB/s); not the benchmark line")
+    ap.add_argument("--sweep-path", type=int, default=0,
+                    help="with --rows-sweep: also a forced kernel family (ggrn_path id)")
     args = ap.parse_args(argv)
     _, world, _ = dist_env()
     if world != args.gpus and args.gpus != 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
-    if args.impl == "reference":
+    if args.rows_sweep:
+        if args.steps > 2000:
+            args.steps = 1000
+        run_rows_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -55,6 +55,7 @@ constexpr int kStraddleBlock = 256;
 constexpr int kScalarBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;
 constexpr int kStreamWarps = 8;                 // consumer warps per CTA (target)
+constexpr int kStreamWarpsPaired = 12;          // ... for 4-lane x 7-vector paired items
 constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
 // Two CTAs per SM, 8 consumer warps, a double-buffered ring: the best of a
 // sweep over 1-2 CTAs/SM, 6-16 consumer warps and 2-4 stages on the prefill
@@ -322,7 +323,17 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   const int se = sv / es;
   const int64_t nvec = Q * a.gs / se;     // vectors per item
   if (nvec < 4 || nvec > 128) return GGRN_ERR_UNSUPPORTED;
-  const int lanes = next_pow2(static_cast<int>(ceil_div(nvec, 4)));
+  int lanes = next_pow2(static_cast<int>(ceil_div(nvec, 4)));
+  int vpl = 4;
+  int target_warps = kStreamWarps;
+  if (Q == 2 && nvec > 16 && nvec <= 28) {
+    // a pair of 17..28 vectors (25 for the 100-wide bf16 odd span): 4 lanes x
+    // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25); more
+    // consumer warps carry the extra registers (measured best: 12)
+    lanes = 4;
+    vpl = 7;
+    target_warps = kStreamWarpsPaired;
+  }
   const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass
   const int64_t gpr = a.width / a.gs;
   const int64_t total = a.rows * gpr;
@@ -333,7 +344,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   if (flat) {
     // consecutive groups of the contiguous [rows * width] data
     mode = 0;
-    W = kStreamWarps;
+    W = target_warps;
     ug = W * gpw;
     units = ceil_div(total, ug);
     const int64_t last = total - (units - 1) * ug;
@@ -343,7 +354,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
     for (int w = 4; w <= 16; ++w) {
       const int64_t u = w * gpw;
       if (gpr % u != 0 || (u * gbytes) % 16 != 0) continue;
-      if (W == 0 || std::abs(w - kStreamWarps) <= std::abs(W - kStreamWarps)) W = w;
+      if (W == 0 || std::abs(w - target_warps) <= std::abs(W - target_warps)) W = w;
     }
     if (W != 0) {
       mode = 1;
@@ -354,7 +365,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
       // short rows: whole rows per unit, each row copied on its own
       if ((a.width * es) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
       mode = 2;
-      rpu = std::max<int64_t>(1, (kStreamWarps * gpw) / gpr);
+      rpu = std::max<int64_t>(1, (target_warps * gpw) / gpr);
       W = static_cast<int>(ceil_div(rpu * gpr, gpw));
       if (W > 16) return GGRN_ERR_UNSUPPORTED;
       ug = rpu * gpr;
@@ -391,7 +402,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->smem_vec_bytes = sv;
   p->items_groups = Q;
   p->nvec = static_cast<int>(nvec);
-  p->vpl = 4;
+  p->vpl = vpl;
   p->lanes = lanes;
   p->consumer_warps = W;
   p->ug = static_cast<int>(ug);
@@ -420,10 +431,12 @@ int make_plan(const Args& a, int path, Plan* p) {
   switch (path) {
     case kAuto: {
       if (vec_ok) {
-        // streaming for groups of whole 16-byte vectors; odd spans (paired
-        // items leave a quarter of the lane slots idle) measured faster on
-        // the register-resident straddle family
-        if (plan_stream(a, p, false) == GGRN_OK && p->smem_vec_bytes == 16 && p->items_groups == 1)
+        // streaming for groups of whole 16-byte vectors, and for paired
+        // items of 17..28 vectors (the low-waste 4 x 7 layout); other paired
+        // items leave a quarter of the lane slots idle and measured faster on
+        // the register-resident families
+        if (plan_stream(a, p, false) == GGRN_OK && p->smem_vec_bytes == 16 &&
+            (p->items_groups == 1 || p->vpl == 7))
           return GGRN_OK;
         *p = Plan();
         if (plan_team(a, p) == GGRN_OK) return GGRN_OK;

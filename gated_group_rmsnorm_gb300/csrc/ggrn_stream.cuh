@@ -468,6 +468,8 @@ cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
 
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s) {
+  if (p.smem_vec_bytes == 16 && p.items_groups == 2 && p.lanes == 4 && p.vpl == 7)
+    return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2>>(k, p, s);
   if (p.vpl != 4) return cudaErrorInvalidConfiguration;
   if (p.smem_vec_bytes == 16 && p.items_groups == 1) return launch_stream_sv<T, MODE, 16, 1>(k, p, s);
   if (p.smem_vec_bytes == 16 && p.items_groups == 2) return launch_stream_sv<T, MODE, 16, 2>(k, p, s);

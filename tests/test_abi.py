@@ -128,20 +128,19 @@ def test_plan_selects_families():
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
-    # 9664: register-resident teams of 8 lanes x 4 vectors take pairs of
-    # groups (25 whole 16-byte vectors), 24 pairs per row
+    # 9664: streamed in pairs of groups (25 whole 16-byte vectors) by teams of
+    # 4 lanes x 7 vectors; units of 4 whole rows (12 consumer warps x 8 teams
+    # x 2 groups = 192 groups), one CTA per SM
     p = _plan(65536, 4800, 100, 2, ys=9664)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
+        (g.PATH_STREAM, 4, 7, 65536 // 4, 13 * 32, 152)
+    # register-resident teams of 8 lanes x 4 vectors, 24 pairs per row
+    p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 8, 4, 24 * 65536)
     # the straddle family: one warp per chunk of 5 periods (lcm(100, 8) = 200
     # elements = 25 vectors) in 128 slots, 5 chunks per row
     p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STRADDLE)
     assert (p.path, p.block_threads, p.vec_per_lane, p.items) == (g.PATH_STRADDLE, 256, 4, 5 * 65536)
-    # forced onto the streaming family: paired groups, 25 16-byte vectors per
-    # pair (8 lanes x 4), one 48-group row per unit (6 consumer warps x 4
-    # teams x 2 groups)
-    p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STREAM)
-    assert (p.path, p.team_lanes, p.elems_per_vec, p.items, p.block_threads) == \
-        (g.PATH_STREAM, 8, 8, 65536, 7 * 32)
     # a group of 12 bf16 (24 bytes): 8-byte shared-memory vectors are not
     # chosen automatically; forced streaming pairs the groups (3 vectors per
     # pair is below 4, so it is refused)
