@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstdlib>
@@ -23,6 +24,16 @@
 // Device status word of the library (one per device): kernels whose bounded
 // waits run out set bits here (see ggrn_fault_status).
 __device__ unsigned int g_ggrn_fault;
+
+// Unit-claim words of the streaming kernel's dynamic schedule (epoch << 32 |
+// next unit; see claim_resolve).  Launches take the slots round robin, so
+// launches running at the same time on different streams normally use
+// different words; when two do share one, the epochs keep both complete.
+// Zero (epoch 0, never given to a launch) at module load.
+constexpr int kSchedSlots = 64;
+// Claimed indices are 32-bit: larger launches take the static schedule.
+constexpr int64_t kMaxClaimUnits = int64_t{1} << 30;
+__device__ unsigned long long g_ggrn_sched[kSchedSlots];
 
 namespace ggrn {
 namespace {
@@ -43,6 +54,31 @@ unsigned int* fault_word() {
     cache[dev] = static_cast<unsigned int*>(ptr);
   }
   return cache[dev];
+}
+
+// Address of this device's claim words (looked up once per device).
+unsigned long long* sched_words() {
+  static std::mutex mu;
+  static unsigned long long* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_ggrn_sched) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned long long*>(ptr);
+  }
+  return cache[dev];
+}
+
+// A new claim epoch per launch (nonzero; wraps after 2^32 - 1 launches).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e;
+  do {
+    e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);
+  return e;
 }
 
 constexpr int kDefaultSMs = 152;
@@ -301,6 +337,32 @@ int plan_scalar(const Args& a, Plan* p) {
   return GGRN_OK;
 }
 
+// Shared memory of the streaming kernels: choose CTAs per SM (2, else 1) and
+// ring stages (2..max_stages) for stage slots of `stage_bytes`, staging the
+// weight (`wb` bytes) when it is a 16-byte multiple and leaves room for the
+// ring.  False when not even two stages fit.
+bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t max_stages, int* cps, int* ns,
+                 int64_t* wstage) {
+  *cps = 0;
+  *ns = 0;
+  *wstage = 0;
+  for (int staged = 1; staged >= 0 && *ns < 2; --staged) {
+    const int64_t warea = staged ? ceil_div(wb, 128) * 128 : 0;
+    if (staged && (wb % 16 != 0 || wb > kStreamMaxWeightBytes)) continue;
+    for (int c = 2; c >= 1; --c) {
+      const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 256;
+      const int64_t n = std::min<int64_t>(max_stages, budget / (2 * stage_bytes));
+      if (n >= 2) {
+        *cps = c;
+        *ns = static_cast<int>(n);
+        *wstage = staged ? wb : 0;
+        break;
+      }
+    }
+  }
+  return *ns >= 2;
+}
+
 // STREAM: persistent CTAs fed by bulk copies of row chunks ("units" of ug
 // whole groups).  A team takes an item of Q groups: Q = 1 when a group's
 // bytes are a multiple of 16 (or of 8, with 8-byte shared-memory vectors),
@@ -334,6 +396,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
     vpl = 7;
     target_warps = kStreamWarpsPaired;
   }
+  const int wmax = vpl == 7 ? kStreamMaxWarps4x7 : kStreamMaxWarps;
   const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass
   const int64_t gpr = a.width / a.gs;
   const int64_t total = a.rows * gpr;
@@ -351,7 +414,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
     if ((ug * gbytes) % 16 != 0 || (last * gbytes) % 16 != 0) return GGRN_ERR_UNSUPPORTED;
   } else {
     // units inside a row: ug = W * gpw must divide the row's groups
-    for (int w = 4; w <= 16; ++w) {
+    for (int w = 4; w <= wmax; ++w) {
       const int64_t u = w * gpw;
       if (gpr % u != 0 || (u * gbytes) % 16 != 0) continue;
       if (W == 0 || std::abs(w - target_warps) <= std::abs(W - target_warps)) W = w;
@@ -367,7 +430,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
       mode = 2;
       rpu = std::max<int64_t>(1, (target_warps * gpw) / gpr);
       W = static_cast<int>(ceil_div(rpu * gpr, gpw));
-      if (W > 16) return GGRN_ERR_UNSUPPORTED;
+      if (W > wmax) return GGRN_ERR_UNSUPPORTED;
       ug = rpu * gpr;
       units = ceil_div(a.rows, rpu);
     }
@@ -376,26 +439,13 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   // The weight is staged in shared memory once per CTA when its bytes are a
   // 16-byte multiple and it leaves room for the ring.
   const int64_t wb = a.mode == kMamba2 ? a.width * 4 : a.gs * es;
-  int cps = 0, ns = 0;
-  int64_t wstage = 0;
-  for (int staged = 1; staged >= 0 && ns < 2; --staged) {
-    const int64_t warea = staged ? ceil_div(wb, 128) * 128 : 0;
-    if (staged && (wb % 16 != 0 || wb > kStreamMaxWeightBytes)) continue;
-    for (int c = 2; c >= 1; --c) {
-      const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 256;
-      const int64_t n = std::min<int64_t>(kStreamMaxStages, budget / (2 * stage_bytes));
-      if (n >= 2) {
-        cps = c;
-        ns = static_cast<int>(n);
-        wstage = staged ? wb : 0;
-        break;
-      }
-    }
-  }
-  if (ns < 2) return GGRN_ERR_UNSUPPORTED;
+  int cps, ns;
+  int64_t wstage;
+  if (!stream_smem(stage_bytes, wb, kStreamMaxStages, &cps, &ns, &wstage))
+    return GGRN_ERR_UNSUPPORTED;
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
   if (!forced && units < 2 * gmax) return GGRN_ERR_UNSUPPORTED;
-  // equal units per CTA: the last wave ends together
+  // static schedule: equal units per CTA, so the last wave ends together
   const int64_t per_cta = ceil_div(units, gmax);
   p->path = kStream;
   p->elems_per_vec = se;
@@ -415,11 +465,14 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->stage_bytes = stage_bytes;
   p->stages = ns;
   p->ctas_per_sm = cps;
-  p->grid = ceil_div(units, per_cta);
+  // dynamic schedule (claimed units): every CTA slot of the device
+  p->grid = std::min(units, gmax);
+  p->grid_static = ceil_div(units, per_cta);
   p->block = (W + 1) * 32;
   p->w_smem_bytes = static_cast<uint32_t>(wstage);
+  // ring, weight, barriers full/empty/weight, unit of each stage
   p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes +
-                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 1));
+                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 1) + 8 * ns);
   p->div_magic = mode == 1 ? div_magic(units, upr) : 0;
   p->div_magic2 = div_magic(total, gpr);
   return GGRN_OK;
@@ -485,12 +538,35 @@ Args make_args(const void* y, const void* gate, const void* w, void* out, int64_
   return a;
 }
 
-int launch(const Args& a, const Plan& p, cudaStream_t s) {
-  if (p.grid == 0) return GGRN_OK;
+// Is work enqueued on `s` being recorded into a graph?  (An error of the
+// query counts as yes: the static schedule is always safe.)
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+int launch(const Args& a, const Plan& plan, cudaStream_t s) {
+  if (plan.grid == 0) return GGRN_OK;
+  Plan p = plan;
   KParams k = make_params(a, p);
   if (p.path == kStream) {
     k.fault = fault_word();
     if (!k.fault) return GGRN_ERR_CUDA;
+    // A graph replays its launches with the parameters they were recorded
+    // with, the claim epoch included: recorded launches take the static
+    // schedule.
+    if (capturing(s) || p.items > kMaxClaimUnits) {
+      p.grid = p.grid_static;
+    } else {
+      unsigned long long* words = sched_words();
+      if (!words) return GGRN_ERR_CUDA;
+      k.epoch = next_epoch();
+      k.sched = words + (k.epoch % kSchedSlots);
+    }
   }
   cudaError_t e;
   switch (a.dtype) {
@@ -554,6 +630,8 @@ KParams make_params(const Args& a, const Plan& p) {
   k.rows_per_unit = p.rows_per_unit;
   k.rows = a.rows;
   k.fault = nullptr;
+  k.sched = nullptr;
+  k.epoch = 0;
   k.eps = a.eps;
   k.gs_f = static_cast<float>(a.gs);
   return k;
@@ -623,7 +701,8 @@ extern "C" int ggrn_graph_create(const ggrn_call* calls, int32_t n, void** graph
     Plan p;
     if (a.rows > 0 && (st = make_plan(a, kAuto, &p)) != GGRN_OK) return st;
   }
-  if (!fault_word()) return GGRN_ERR_CUDA;  // symbol lookup before the capture starts
+  // symbol lookups before the capture starts
+  if (!fault_word() || !sched_words()) return GGRN_ERR_CUDA;
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GGRN_ERR_CUDA;
   int status = GGRN_OK;

@@ -32,6 +32,7 @@ struct Plan {
   int block = 0;        // threads per CTA
   int smem = 0;         // dynamic shared memory bytes
   int64_t grid = 0;     // CTAs
+  int64_t grid_static = 0;  // STREAM: CTAs of the static schedule (graph capture)
   int64_t items = 0;    // groups, row chunks (STRADDLE) or units (STREAM)
   int64_t groups = 0;   // groups per row
   int64_t items_per_row = 0;  // TEAM: items (groups or pairs of groups) per row
@@ -59,6 +60,11 @@ struct Plan {
   uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
   int ctas_per_sm = 0;
 };
+
+// Most consumer warps of a streaming launch (the kernels' launch bounds):
+// 4-lane x 7-vector paired items need more registers, hence fewer warps.
+constexpr int kStreamMaxWarps = 16;
+constexpr int kStreamMaxWarps4x7 = 12;
 
 // Kernel parameters (passed by value).
 struct KParams {
@@ -92,6 +98,8 @@ struct KParams {
   int unit_mode;
   int rows_per_unit;
   int64_t rows;
+  unsigned long long* sched;  // STREAM: unit-claim word, or NULL (static schedule)
+  uint32_t epoch;             // STREAM: this launch's claim epoch (nonzero)
   float eps;
   float gs_f;
 };

@@ -17,6 +17,14 @@
 // (the odd span of 100 bf16 = 200 bytes) be read at group granularity with no
 // straddling: the bulk copy itself moves 16-byte-multiple chunks.
 //
+// Schedule: each CTA takes its first NS units statically (CTA b: units b,
+// b + grid, ...), then claims units one at a time from a word in device
+// memory shared by the CTAs of the launch, so that CTAs that run slower
+// (memory-channel contention varies) take fewer units and all finish within
+// about one unit of each other.  The claim of the next unit is issued while
+// the producer waits for a free stage.  Launches recorded into a CUDA graph
+// keep the static interleaved schedule (no claim word).
+//
 // Waits are bounded: after kWaitLimit polls a thread records a fault bit in
 // the library's device status word and stops; the producer lane then waits
 // (again bounded) until every copy it issued has landed, so no copy targets
@@ -35,6 +43,9 @@ constexpr uint32_t kWaitHintNs = 1000;
 constexpr uint32_t kFaultConsumerWait = 1u;
 constexpr uint32_t kFaultProducerWait = 2u;
 constexpr uint32_t kFaultDrainWait = 4u;
+constexpr uint32_t kFaultClaim = 8u;
+// Attempts of one unit claim against other launches' installations.
+constexpr uint32_t kClaimTries = 4096;
 // Unit shapes: ug consecutive groups of contiguous rows (flat), ug groups
 // inside one row (chunk), or rows_per_unit whole rows copied row by row.
 constexpr int kUnitFlat = 0;
@@ -158,106 +169,259 @@ __device__ __forceinline__ void round_to_t(float* f) {
 }
 
 // ---------------------------------------------------------------------------
+// Unit claims.  The claim word holds epoch << 32 | next: the launch whose
+// epoch (a number the host gives each launch) is installed hands out indices
+// 0, 1, 2, ... in order, one per atomicAdd.  `v` is what the caller's
+// atomicAdd(w, 1) returned.  A word carrying another epoch (the slot's
+// previous launch, or a concurrent launch given the same slot) is replaced
+// by this epoch with next = 1, the caller taking index 0.  A launch whose
+// installation was replaced installs itself again and restarts at 0: units
+// may then be processed twice (the same bytes written again) but none is
+// skipped, since a CTA stops only on an index >= the count under its own
+// launch's latest installation, all lower indices of which went to CTAs of
+// that launch.  Returns the index, or -1 (and *ok = false) after
+// kClaimTries attempts.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t claim_resolve(unsigned long long* w, uint32_t epoch,
+                                                 unsigned long long v, bool* ok) {
+  const unsigned long long fresh = (static_cast<unsigned long long>(epoch) << 32) | 1ull;
+  unsigned long long cur = v + 1;  // the word as the caller's add left it
+  for (uint32_t t = 0; t < kClaimTries; ++t) {
+    if (static_cast<uint32_t>(v >> 32) == epoch) return static_cast<int64_t>(v & 0xffffffffull);
+    const unsigned long long seen = atomicCAS(w, cur, fresh);
+    if (seen == cur) return 0;
+    if (static_cast<uint32_t>(seen >> 32) == epoch) {
+      v = atomicAdd(w, 1ull);  // installed by another CTA: claim normally
+      cur = v + 1;
+    } else {
+      cur = seen;  // still another epoch's word: try to replace what is there now
+    }
+  }
+  *ok = false;
+  return -1;
+}
+
+// ---------------------------------------------------------------------------
+// Pieces of the streaming kernel.  Dynamic shared memory:
+// [stages][y slot | gate slot], the weight area, then the barriers
+// full[NS], empty[NS], wbar, and the unit of each stage (int64 [NS]).
+// ---------------------------------------------------------------------------
+struct StreamCtx {
+  unsigned char* ring;
+  unsigned char* wsm;    // staged weight (when wbytes != 0)
+  long long* unit_of;    // unit in each stage; -1: no more units
+  uint32_t sb;           // bytes of one tensor's slot (128-aligned)
+  uint32_t wbytes;       // 0: the weight is read from global memory
+  uint32_t full0, empty0, wbar;
+  int NS, W;
+};
+
+// Barrier set-up (thread 0), then the programmatic-dependent-launch wait:
+// nothing global is touched before the previous kernel's writes are visible.
+__device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned char* smem) {
+  StreamCtx c;
+  c.ring = smem;
+  c.NS = p.stages;
+  c.W = p.consumer_warps;
+  c.sb = p.stage_bytes;
+  c.wsm = smem + static_cast<size_t>(2) * c.NS * c.sb;
+  c.wbytes = p.w_smem_bytes;
+  const uint32_t warea = (c.wbytes + 127u) & ~127u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(c.wsm + warea);
+  c.full0 = smem_u32(bars);
+  c.empty0 = smem_u32(bars + c.NS);
+  c.wbar = smem_u32(bars + 2 * c.NS);
+  c.unit_of = reinterpret_cast<long long*>(bars + 2 * c.NS + 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < c.NS; ++s) {
+      mbar_init(c.full0 + 8 * s, 1);
+      mbar_init(c.empty0 + 8 * s, c.W);
+    }
+    mbar_init(c.wbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  return c;
+}
+
+// The producer lane: stage the weight, then stream this CTA's units into the
+// ring, each stage's unit recorded in unit_of; after the last unit a stage
+// with unit -1 (completed by a plain arrive) tells the consumers to stop.
+// Finally wait (bounded) until every issued copy has landed.
+template <typename T>
+__device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx& c) {
+  constexpr int ES = sizeof(T);
+  const int64_t gs = p.gs;
+  if (c.wbytes) {
+    mbar_expect_tx(c.wbar, c.wbytes);
+    bulk_g2s(smem_u32(c.wsm), p.w, c.wbytes, c.wbar);
+  }
+  const int NS = c.NS;
+  const int64_t G = gridDim.x;
+  const bool dyn = p.sched != nullptr;
+  int64_t i = 0;
+  bool ok = true, claim_ok = true;
+  unsigned long long pending = 0;  // the claim issued for the next stage
+  int64_t u = blockIdx.x;
+  for (;; ++i) {
+    const int s = static_cast<int>(i % NS);
+    if (i >= NS && !mbar_wait(c.empty0 + 8 * s, static_cast<uint32_t>((i / NS) - 1) & 1u)) {
+      ok = false;
+      break;
+    }
+    if (dyn && i >= NS) {
+      const int64_t d = claim_resolve(p.sched, p.epoch, pending, &claim_ok);
+      u = claim_ok ? NS * G + d : p.units;
+    }
+    const uint32_t full = c.full0 + 8 * s;
+    if (u >= p.units) {
+      c.unit_of[s] = -1;
+      mbar_arrive(full);
+      ++i;
+      break;
+    }
+    c.unit_of[s] = u;
+    unsigned char* st = c.ring + static_cast<size_t>(2) * s * c.sb;
+    if (p.unit_mode == kUnitRows) {
+      // R whole rows, one copy per row and tensor, packed in the slot
+      const int64_t row0 = u * p.rows_per_unit;
+      const int64_t nr = min(static_cast<int64_t>(p.rows_per_unit), p.rows - row0);
+      const uint32_t rb = static_cast<uint32_t>(p.width * ES);
+      mbar_expect_tx(full, static_cast<uint32_t>(2 * nr) * rb);
+      for (int64_t r = 0; r < nr; ++r) {
+        bulk_g2s(smem_u32(st + r * rb), static_cast<const T*>(p.y) + (row0 + r) * p.ys, rb, full);
+        bulk_g2s(smem_u32(st + c.sb + r * rb), static_cast<const T*>(p.gate) + (row0 + r) * p.gts,
+                 rb, full);
+      }
+    } else {
+      int64_t yo, go, ngroups;
+      if (p.unit_mode == kUnitFlat) {
+        const int64_t g0 = u * p.ug;
+        ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - g0);
+        yo = go = g0 * gs;
+      } else {
+        const int64_t row = div_by(u, p.units_per_row, p.div_magic);
+        const int64_t c0 = (u - row * p.units_per_row) * p.ug * gs;
+        ngroups = p.ug;
+        yo = row * p.ys + c0;
+        go = row * p.gts + c0;
+      }
+      const uint32_t bytes = static_cast<uint32_t>(ngroups * gs * ES);
+      mbar_expect_tx(full, 2 * bytes);
+      bulk_g2s(smem_u32(st), static_cast<const T*>(p.y) + yo, bytes, full);
+      bulk_g2s(smem_u32(st + c.sb), static_cast<const T*>(p.gate) + go, bytes, full);
+    }
+    if (dyn && i + 1 >= NS) {
+      pending = atomicAdd(p.sched, 1ull);  // resolved after the next empty wait
+    } else {
+      u += G;
+    }
+  }
+  if (!ok) atomicOr(p.fault, kFaultProducerWait);
+  if (!claim_ok) atomicOr(p.fault, kFaultClaim);
+  // Every issued copy lands before this thread leaves: wait for the last
+  // phase of each stage used (already complete in the normal course).
+  const int64_t n_issued = i;
+  for (int s = 0; s < NS && s < n_issued; ++s) {
+    const int64_t last = s + ((n_issued - 1 - s) / NS) * NS;
+    if (!mbar_wait(c.full0 + 8 * s, static_cast<uint32_t>(last / NS) & 1u))
+      atomicOr(p.fault, kFaultDrainWait);
+  }
+  if (c.wbytes && !mbar_wait(c.wbar, 0)) atomicOr(p.fault, kFaultDrainWait);
+}
+
+// A unit's first group (flattened, flat units), its group count, and its row
+// and column origin (chunk and row units).
+struct UnitPos {
+  int64_t g0, ngroups, row, col;
+};
+__device__ __forceinline__ UnitPos unit_pos(const KParams& p, int64_t u) {
+  UnitPos r{0, 0, 0, 0};
+  if (p.unit_mode == kUnitFlat) {
+    r.g0 = u * p.ug;
+    r.ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - r.g0);
+  } else if (p.unit_mode == kUnitChunk) {
+    r.row = div_by(u, p.units_per_row, p.div_magic);
+    r.col = (u - r.row * p.units_per_row) * p.ug * p.gs;
+    r.ngroups = p.ug;
+  } else {
+    r.row = u * p.rows_per_unit;
+    r.ngroups = min(static_cast<int64_t>(p.rows_per_unit), p.rows - r.row) * p.groups;
+  }
+  return r;
+}
+
+// Output offset (elements) and weight column of group gl of a unit.
+__device__ __forceinline__ void group_place(const KParams& p, const UnitPos& up, int gl,
+                                            int64_t* out_off, int64_t* wcol) {
+  const int64_t gs = p.gs;
+  if (p.unit_mode == kUnitFlat) {
+    const int64_t G = up.g0 + gl;
+    *out_off = G * gs;  // flat: out rows are contiguous
+    const int64_t row = div_by(G, p.groups, p.div_magic2);
+    *wcol = (G - row * p.groups) * gs;
+  } else if (p.unit_mode == kUnitChunk) {
+    *out_off = up.row * p.os + up.col + gl * gs;
+    *wcol = up.col + gl * gs;
+  } else {
+    const int r = gl / static_cast<int>(p.groups);  // row within the unit
+    *wcol = (gl - r * p.groups) * gs;
+    *out_off = (up.row + r) * p.os + *wcol;
+  }
+}
+
+// f32 weight of SE columns at wi (shared memory when staged).
+template <int SE>
+__device__ __forceinline__ void load_w_cols(const KParams& p, const StreamCtx& c, int64_t wi,
+                                            float (&wv)[SE]) {
+#pragma unroll
+  for (int q = 0; q < SE; q += 4 > SE ? SE : 4) {
+    if (SE >= 4) {
+      const float4 w4 =
+          c.wbytes ? *reinterpret_cast<const float4*>(c.wsm + 4 * (wi + q))
+                   : __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.w) + wi + q));
+      wv[q] = w4.x, wv[(q + 1) % SE] = w4.y, wv[(q + 2) % SE] = w4.z, wv[(q + 3) % SE] = w4.w;
+    } else {
+      const float2 w2 =
+          c.wbytes ? *reinterpret_cast<const float2*>(c.wsm + 4 * (wi + q))
+                   : __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(p.w) + wi + q));
+      wv[q] = w2.x, wv[(q + 1) % SE] = w2.y;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // k_stream: TEAM consumers.  SV = bytes per shared-memory vector (16 or 8),
 // SE = elements per vector, L lanes per team, VPL vectors per lane, Q groups
-// per team item (1, or 2 for groups of an odd number of half vectors).
-// Dynamic shared memory: [stages][y chunk | gate chunk] then the barriers.
+// per team item (1, or 2 for groups of an odd number of half vectors), MAXW
+// the most consumer warps a launch may have (it sets the register budget:
+// 17 warps leave 96 registers a thread, 13 leave 128).
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, int L, int VPL, int SV, int Q>
-__global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
+template <typename T, int MODE, int L, int VPL, int SV, int Q, int MAXW>
+__global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) {
   constexpr int ES = sizeof(T);
   constexpr int SE = SV / ES;
   constexpr int NW = SV / 4;
   constexpr int TPW = 32 / L;  // teams (items) per warp
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int W = p.consumer_warps;
-  const int NS = p.stages;
-  const uint32_t sb = p.stage_bytes;  // bytes of one tensor's chunk slot (128-aligned)
+  const StreamCtx c = stream_setup(p, smem);
+  const int W = c.W;
+  const int NS = c.NS;
+  const uint32_t sb = c.sb;
+  const uint32_t wbytes = c.wbytes;
+  unsigned char* wsm = c.wsm;
+  const uint32_t full0 = c.full0, empty0 = c.empty0;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // The weight (MAMBA2 f32 [width], ONNX scale [C]) is staged once per CTA
-  // after the ring when it fits: every unit then reads it from shared memory.
-  unsigned char* wsm = smem + static_cast<size_t>(2) * NS * sb;
-  const uint32_t wbytes = p.w_smem_bytes;                 // 0: read from global
-  const uint32_t warea = (wbytes + 127u) & ~127u;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + warea);
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + NS);
-  const uint32_t wbar = smem_u32(bars + 2 * NS);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, W);
-    }
-    mbar_init(wbar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  pdl_wait();
-  pdl_launch_dependents();
-
   const int64_t gs = p.gs;
   if (warp == W) {
-    // ---------------- producer ----------------
-    if (lane != 0) return;
-    if (wbytes) {
-      mbar_expect_tx(wbar, wbytes);
-      bulk_g2s(smem_u32(wsm), p.w, wbytes, wbar);
-    }
-    int64_t i = 0;
-    bool ok = true;
-    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
-      const int s = static_cast<int>(i % NS);
-      if (i >= NS && !mbar_wait(empty0 + 8 * s, static_cast<uint32_t>((i / NS) - 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      const uint32_t full = full0 + 8 * s;
-      unsigned char* st = smem + static_cast<size_t>(2) * s * sb;
-      if (p.unit_mode == kUnitRows) {
-        // R whole rows, one copy per row and tensor, packed in the slot
-        const int64_t row0 = u * p.rows_per_unit;
-        const int64_t nr = min(static_cast<int64_t>(p.rows_per_unit), p.rows - row0);
-        const uint32_t rb = static_cast<uint32_t>(p.width * ES);
-        mbar_expect_tx(full, static_cast<uint32_t>(2 * nr) * rb);
-        for (int64_t r = 0; r < nr; ++r) {
-          bulk_g2s(smem_u32(st + r * rb), static_cast<const T*>(p.y) + (row0 + r) * p.ys, rb, full);
-          bulk_g2s(smem_u32(st + sb + r * rb), static_cast<const T*>(p.gate) + (row0 + r) * p.gts,
-                   rb, full);
-        }
-      } else {
-        int64_t yo, go, ngroups;
-        if (p.unit_mode == kUnitFlat) {
-          const int64_t g0 = u * p.ug;
-          ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - g0);
-          yo = go = g0 * gs;
-        } else {
-          const int64_t row = div_by(u, p.units_per_row, p.div_magic);
-          const int64_t c0 = (u - row * p.units_per_row) * p.ug * gs;
-          ngroups = p.ug;
-          yo = row * p.ys + c0;
-          go = row * p.gts + c0;
-        }
-        const uint32_t bytes = static_cast<uint32_t>(ngroups * gs * ES);
-        mbar_expect_tx(full, 2 * bytes);
-        bulk_g2s(smem_u32(st), static_cast<const T*>(p.y) + yo, bytes, full);
-        bulk_g2s(smem_u32(st + sb), static_cast<const T*>(p.gate) + go, bytes, full);
-      }
-    }
-    if (!ok) atomicOr(p.fault, kFaultProducerWait);
-    // Every issued copy lands before this thread leaves: wait for the last
-    // phase of each stage used (already complete in the normal course).
-    const int64_t n_issued = i;
-    for (int s = 0; s < NS && s < n_issued; ++s) {
-      const int64_t last = s + ((n_issued - 1 - s) / NS) * NS;
-      if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(last / NS) & 1u))
-        atomicOr(p.fault, kFaultDrainWait);
-    }
-    if (wbytes && !mbar_wait(wbar, 0)) atomicOr(p.fault, kFaultDrainWait);
+    if (lane == 0) stream_produce<T>(p, c);
     return;
   }
-  if (wbytes && !mbar_wait(wbar, 0)) {
+  if (wbytes && !mbar_wait(c.wbar, 0)) {
     if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
     return;
   }
@@ -272,48 +436,24 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
   const int nvec = static_cast<int>(Q * gs / SE);
   const int vb = static_cast<int>(gs / SE);
   const int items_per_pass = W * TPW;
-  int64_t i = 0;
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+  for (int64_t i = 0;; ++i) {
     const int s = static_cast<int>(i % NS);
     if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(i / NS) & 1u)) {
       if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
       break;
     }
-    // unit -> first group (flattened) and its row/column origin
-    int64_t g0 = 0, ngroups, row_u = 0, col_u = 0;
-    if (p.unit_mode == kUnitFlat) {
-      g0 = u * p.ug;
-      ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - g0);
-    } else if (p.unit_mode == kUnitChunk) {
-      row_u = div_by(u, p.units_per_row, p.div_magic);
-      col_u = (u - row_u * p.units_per_row) * p.ug * gs;
-      ngroups = p.ug;
-    } else {
-      row_u = u * p.rows_per_unit;
-      ngroups = min(static_cast<int64_t>(p.rows_per_unit), p.rows - row_u) * p.groups;
-    }
-    const int nitems = static_cast<int>(ngroups / Q);
+    const int64_t u = c.unit_of[s];
+    if (u < 0) break;
+    const UnitPos up = unit_pos(p, u);
+    const int nitems = static_cast<int>(up.ngroups / Q);
     const unsigned char* sy = smem + static_cast<size_t>(2) * s * sb;
     const unsigned char* sg = sy + sb;
     for (int pass = 0; pass * items_per_pass < nitems; ++pass) {
       const int item = pass * items_per_pass + warp * TPW + team;
       const bool active = item < nitems;
       const int gl = item * Q;  // first group of the item within the unit
-      // output origin and weight column of that group
-      int64_t out_off, wcol;
-      if (p.unit_mode == kUnitFlat) {
-        const int64_t G = g0 + gl;
-        out_off = G * gs;  // flat: out rows are contiguous
-        const int64_t row = div_by(G, p.groups, p.div_magic2);
-        wcol = (G - row * p.groups) * gs;
-      } else if (p.unit_mode == kUnitChunk) {
-        out_off = row_u * p.os + col_u + gl * gs;
-        wcol = col_u + gl * gs;
-      } else {
-        const int r = gl / static_cast<int>(p.groups);   // row within the unit
-        wcol = (gl - r * p.groups) * gs;
-        out_off = (row_u + r) * p.os + wcol;
-      }
+      int64_t out_off, wcol;    // output origin and weight column of that group
+      group_place(p, up, gl, &out_off, &wcol);
       const unsigned char* gy = sy + static_cast<size_t>(gl) * gs * ES;
       const unsigned char* gg = sg + static_cast<size_t>(gl) * gs * ES;
 
@@ -377,22 +517,7 @@ __global__ void __launch_bounds__(17 * 32, 1) k_stream(const KParams p) {
           float r[SE];
           if (MODE == kMamba2) {
             float wv[SE];
-            const int64_t wi = wcol + v * SE;
-#pragma unroll
-            for (int q = 0; q < SE; q += 4 > SE ? SE : 4) {
-              if (SE >= 4) {
-                const float4 w4 =
-                    wbytes ? *reinterpret_cast<const float4*>(wsm + 4 * (wi + q))
-                           : __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.w) + wi + q));
-                wv[q] = w4.x, wv[(q + 1) % SE] = w4.y, wv[(q + 2) % SE] = w4.z,
-                wv[(q + 3) % SE] = w4.w;
-              } else {
-                const float2 w2 =
-                    wbytes ? *reinterpret_cast<const float2*>(wsm + 4 * (wi + q))
-                           : __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(p.w) + wi + q));
-                wv[q] = w2.x, wv[(q + 1) % SE] = w2.y;
-              }
-            }
+            load_w_cols<SE>(p, c, wcol + v * SE, wv);
 #pragma unroll
             for (int e = 0; e < SE; ++e) r[e] = a[k][e] * (e < SE / 2 ? nlo : nhi);
             round_to_t<T, SE>(r);
@@ -441,12 +566,17 @@ cudaError_t launch_stream_kernel(const KParams& k, const Plan& p, cudaStream_t s
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (p.smem > 48 * 1024 && !(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & bit)) {
-    // the device's whole per-block limit, so later launches of this kernel
-    // with a larger ring need no further call
+    // the device's whole per-block limit less the kernel's static shared
+    // memory, so later launches of this kernel with a larger ring need no
+    // further call
     int limit = 0;
     e = cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             limit - static_cast<int>(fa.sharedSizeBytes));
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&opted_in, bit, __ATOMIC_RELEASE);
   }
@@ -456,12 +586,12 @@ cudaError_t launch_stream_kernel(const KParams& k, const Plan& p, cudaStream_t s
 template <typename T, int MODE, int SV, int Q>
 cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
   switch (p.lanes) {
-    case 1: return launch_stream_kernel<k_stream<T, MODE, 1, 4, SV, Q>>(k, p, s);
-    case 2: return launch_stream_kernel<k_stream<T, MODE, 2, 4, SV, Q>>(k, p, s);
-    case 4: return launch_stream_kernel<k_stream<T, MODE, 4, 4, SV, Q>>(k, p, s);
-    case 8: return launch_stream_kernel<k_stream<T, MODE, 8, 4, SV, Q>>(k, p, s);
-    case 16: return launch_stream_kernel<k_stream<T, MODE, 16, 4, SV, Q>>(k, p, s);
-    case 32: return launch_stream_kernel<k_stream<T, MODE, 32, 4, SV, Q>>(k, p, s);
+    case 1: return launch_stream_kernel<k_stream<T, MODE, 1, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
+    case 2: return launch_stream_kernel<k_stream<T, MODE, 2, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
+    case 4: return launch_stream_kernel<k_stream<T, MODE, 4, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
+    case 8: return launch_stream_kernel<k_stream<T, MODE, 8, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
+    case 16: return launch_stream_kernel<k_stream<T, MODE, 16, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
+    case 32: return launch_stream_kernel<k_stream<T, MODE, 32, 4, SV, Q, kStreamMaxWarps>>(k, p, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -469,7 +599,7 @@ cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s) {
   if (p.smem_vec_bytes == 16 && p.items_groups == 2 && p.lanes == 4 && p.vpl == 7)
-    return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2>>(k, p, s);
+    return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2, kStreamMaxWarps4x7>>(k, p, s);
   if (p.vpl != 4) return cudaErrorInvalidConfiguration;
   if (p.smem_vec_bytes == 16 && p.items_groups == 1) return launch_stream_sv<T, MODE, 16, 1>(k, p, s);
   if (p.smem_vec_bytes == 16 && p.items_groups == 2) return launch_stream_sv<T, MODE, 16, 2>(k, p, s);

@@ -23,10 +23,13 @@
  * Memory.  Every pointer is a DEVICE pointer owned by the caller.  y, gate
  * and out are [rows, width] matrices of T with unit inner stride and the
  * given row strides in ELEMENTS (a strided view split from a fused in-proj
- * output is read in place).  The library allocates no device memory, does
- * not synchronise, and enqueues all work on `cuda_stream` (a cudaStream_t;
+ * output is read in place).  The library allocates no device memory (its
+ * own state is a few module-scope device words per device: the status word
+ * below and the unit-claim words of the STREAM family's schedule), does not
+ * synchronise, and enqueues all work on `cuda_stream` (a cudaStream_t;
  * NULL = the legacy default stream), so calls may be captured in a CUDA
- * graph.  out must not overlap y or gate.
+ * graph (a captured STREAM launch uses the static schedule, which replays
+ * unchanged).  out must not overlap y or gate.
  *
  * Errors.  Argument errors are detected on the host before anything is
  * enqueued and returned synchronously (nothing is launched).  A launch
@@ -186,8 +189,8 @@ int ggrn_version(void);
  * STREAM kernels bound every wait on a shared-memory barrier; a wait that
  * runs out stops the kernel and sets a bit here: 1 = a consumer waited for
  * data, 2 = the producer waited for a free stage, 4 = the producer waited for
- * its copies to land.  Nonzero means the outputs of some call are
- * incomplete.  Synchronises the device, writes the word to *flags and, when
+ * its copies to land, 8 = a unit claim of the dynamic schedule gave up.
+ * Nonzero means the outputs of some call are incomplete.  Synchronises the device, writes the word to *flags and, when
  * `clear` is nonzero, resets it.  Returns GGRN_OK, GGRN_ERR_ARG (flags NULL)
  * or GGRN_ERR_CUDA.
  */

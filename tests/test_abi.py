@@ -110,11 +110,11 @@ def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
 def test_plan_selects_families():
     # Mamba-2 prefill 4096x7680, group 960: streamed, one row (8 groups) per
     # unit, one warp per group (32 lanes x 4 vectors of 16 bytes), 8 consumer
-    # warps + 1 producer warp, 14 units per CTA on 152 SMs x 2 CTAs
+    # warps + 1 producer warp, 2 CTAs on each of 152 SMs claiming units
     p = _plan(4096, 7680, 960, 2)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads) == \
         (g.PATH_STREAM, 32, 4, 4096, 288)
-    assert p.grid_blocks == -(-4096 // 14)
+    assert p.grid_blocks == 2 * 152
     # the same shape on the register-resident family: one warp per group
     p = _plan(4096, 7680, 960, 2, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)

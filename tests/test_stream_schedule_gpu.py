@@ -1,0 +1,115 @@
+"""The streaming family's unit schedule (GPU).
+
+Eager launches claim units dynamically from device words; launches recorded
+into a CUDA graph keep the static interleaved schedule.  Every unit is the
+same computation whichever CTA takes it, so all of these must agree bit for
+bit, and the device status word must stay clear."""
+import pytest
+import torch
+
+import ggrn_inputs
+import gated_group_rmsnorm_gb300 as g
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.load()
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype != torch.float32 else t.view(torch.int32)
+
+
+def _case(name, rows, seed=0):
+    wl = ggrn_inputs.WORKLOADS[name].with_rows(rows)
+    host = ggrn_inputs.make_inputs(wl, seed=seed)
+    return wl, host, gpu_util.to_device(host)
+
+
+def _fwd(wl, dev, out=None):
+    return g.forward(dev.y, dev.gate, dev.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode,
+                     out=out)
+
+
+@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 1500), ("gdn_onnx", 2600),
+                                       ("strided_odd_span", 1900)])
+def test_claimed_schedule_matches_oracle_and_graph_replay(name, rows):
+    g.fault_status(clear=True)
+    wl, host, dev = _case(name, rows)
+    assert g.plan(dev.y, dev.gate, dev.w, group_size=wl.group_size, mode=wl.mode)["path"] == \
+        g.PATH_STREAM
+    eager = _fwd(wl, dev)
+    torch.cuda.synchronize()
+    res = gpu_util.compare(eager, host, wl.group_size, wl.eps, wl.mode)
+    assert res["ok"], res
+    # the same call recorded by torch into a CUDA graph (static schedule)
+    out = torch.empty_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _fwd(wl, dev, out=out)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _fwd(wl, dev, out=out)
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(out), _bits(eager))
+    # the library's own graph API records the static schedule too
+    out2 = torch.empty_like(eager)
+    dg = g.DecodeGraph([dict(y=dev.y, gate=dev.gate, w=dev.w, out=out2, group_size=wl.group_size,
+                             eps=wl.eps, mode=wl.mode)])
+    for _ in range(2):
+        out2.zero_()
+        dg.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(out2), _bits(eager))
+    dg.close()
+    assert g.fault_status() == 0
+
+
+def test_two_streams_at_once():
+    """Launches on two streams overlap on the device; each launch still
+    covers all of its units."""
+    g.fault_status(clear=True)
+    wl_a, _, dev_a = _case("mamba2_prefill", 2048, seed=1)
+    wl_b, _, dev_b = _case("gdn_onnx", 4096, seed=2)
+    ref_a = _fwd(wl_a, dev_a)
+    ref_b = _fwd(wl_b, dev_b)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs_a = [torch.empty_like(ref_a) for _ in range(12)]
+    outs_b = [torch.empty_like(ref_b) for _ in range(12)]
+    for oa, ob in zip(outs_a, outs_b):
+        with torch.cuda.stream(sa):
+            _fwd(wl_a, dev_a, out=oa)
+        with torch.cuda.stream(sb):
+            _fwd(wl_b, dev_b, out=ob)
+    torch.cuda.synchronize()
+    for oa in outs_a:
+        assert torch.equal(_bits(oa), _bits(ref_a))
+    for ob in outs_b:
+        assert torch.equal(_bits(ob), _bits(ref_b))
+    assert g.fault_status() == 0
+
+
+def test_many_launches_cycle_the_claim_words():
+    """More launches than claim words: every word is reused by later
+    launches, each of which replaces the previous launch's epoch."""
+    g.fault_status(clear=True)
+    wl, _, dev = _case("mamba2_prefill", 700, seed=3)
+    ref = _fwd(wl, dev)
+    outs = [torch.empty_like(ref) for _ in range(4)]
+    for i in range(200):
+        _fwd(wl, dev, out=outs[i % 4])
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(_bits(o), _bits(ref))
+    assert g.fault_status() == 0
