@@ -16,7 +16,8 @@ import torch
 from . import build as _build
 
 # ggrn_status
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_OVERLAP, ERR_CUDA, ERR_UNSUPPORTED, ERR_ARG = range(9)
+(OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_OVERLAP, ERR_CUDA, ERR_UNSUPPORTED, ERR_ARG,
+ ERR_LIMIT) = range(10)
 # ggrn_dtype / ggrn_mode / ggrn_path
 F32, F16, BF16 = 0, 1, 2
 MAMBA2, ONNX = 0, 1
@@ -29,7 +30,7 @@ MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 # The exported symbols, as include/ggrn.h declares them.
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
-           "ggrn_fault_status", "ggrn_last_cuda_error")
+           "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc")
 
 
 class GgrnError(RuntimeError):
@@ -84,6 +85,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
         L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
         L.ggrn_forward.restype = ci
+        L.ggrn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci,
+                                           ci, vp]
+        L.ggrn_forward_noalloc.restype = ci
         L.ggrn_forward_path.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci,
                                         ci, vp]
         L.ggrn_forward_path.restype = ci
@@ -129,6 +133,13 @@ def ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride, gate_ro
                  out_row_stride, eps, dtype, mode, stream) -> int:
     return load().ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride,
                                gate_row_stride, out_row_stride, eps, dtype, mode, stream)
+
+
+def ggrn_forward_noalloc(y, gate, w, out, rows, width, group_size, y_row_stride,
+                         gate_row_stride, out_row_stride, eps, dtype, mode, stream) -> int:
+    """The allocation-free streaming entry point (include/ggrn.h documents when to use it)."""
+    return load().ggrn_forward_noalloc(y, gate, w, out, rows, width, group_size, y_row_stride,
+                                       gate_row_stride, out_row_stride, eps, dtype, mode, stream)
 
 
 def ggrn_forward_path(y, gate, w, out, rows, width, group_size, y_row_stride, gate_row_stride,

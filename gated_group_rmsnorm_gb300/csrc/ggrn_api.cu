@@ -763,6 +763,8 @@ extern "C" const char* ggrn_status_string(int status) {
     case GGRN_ERR_CUDA: return "CUDA runtime error";
     case GGRN_ERR_UNSUPPORTED: return "the requested path does not cover this shape";
     case GGRN_ERR_ARG: return "invalid argument (path id, NULL out-parameter or call list)";
+    case GGRN_ERR_LIMIT: return "beyond the fixed limit of ggrn_forward_noalloc (more streamed "
+                                "units than its claim counter can address)";
     default: return "unknown status";
   }
 }
@@ -785,4 +787,89 @@ extern "C" int ggrn_fault_status(uint32_t* flags, int clear) {
 
 extern "C" const char* ggrn_last_cuda_error(void) {
   return cudaGetErrorName(tl_last_cuda_error);
+}
+
+// ---------------------------------------------------------------------------
+// ggrn_forward_noalloc: the streaming kernel with its claim counter in a
+// fixed array of this file (no counterpart in the pages; see include/ggrn.h).
+// ---------------------------------------------------------------------------
+
+// The entry point's scratch: GGRN_NOALLOC_SCRATCH_BYTES in this module, one
+// copy on every device that loads the library, held until the process exits.
+// Word 0 is the unit-claim counter of the call in flight; every call clears
+// it on its own stream before its kernel starts, so calls that overlap on the
+// GPU share it and race.
+static __device__ __align__(256) unsigned long long
+    g_ggrn_noalloc_scratch[GGRN_NOALLOC_SCRATCH_BYTES / sizeof(unsigned long long)];
+
+namespace ggrn {
+namespace {
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// (once per device, on the first call there, with that device current) and
+// passed to the kernel.
+unsigned long long* noalloc_scratch() {
+  static std::mutex mu;
+  static unsigned long long* cache[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    tl_last_cuda_error = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_ggrn_noalloc_scratch);
+    if (e != cudaSuccess) {
+      tl_last_cuda_error = e;
+      return nullptr;
+    }
+    cache[dev] = static_cast<unsigned long long*>(ptr);
+  }
+  return cache[dev];
+}
+
+}  // namespace
+}  // namespace ggrn
+
+extern "C" int ggrn_forward_noalloc(const void* y, const void* gate, const void* w, void* out,
+                                    int64_t rows, int64_t width, int64_t group_size,
+                                    int64_t y_row_stride, int64_t gate_row_stride,
+                                    int64_t out_row_stride, float eps, int dtype, int mode,
+                                    void* cuda_stream) {
+  const Args a = make_args(y, gate, w, out, rows, width, group_size, y_row_stride,
+                           gate_row_stride, out_row_stride, eps, dtype, mode);
+  int st = validate(a);
+  if (st != GGRN_OK || a.rows == 0) return st;
+  if (!vector_layout_ok(a)) return GGRN_ERR_ALIGN;
+  Plan p;
+  st = plan_stream(a, &p, /*forced=*/true);
+  if (st != GGRN_OK) return st;
+  // The counter hands out 32-bit unit indices.
+  if (p.items > GGRN_NOALLOC_MAX_UNITS) return GGRN_ERR_LIMIT;
+  unsigned long long* scratch = noalloc_scratch();
+  if (!scratch) return GGRN_ERR_CUDA;
+  unsigned int* fault = fault_word();
+  if (!fault) return GGRN_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  // Claims start at 0 under epoch 0 (a cleared word reads as installed).
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(unsigned long long), s);
+  if (e == cudaSuccess) {
+    KParams k = make_params(a, p);
+    k.fault = fault;
+    k.sched = scratch;
+    k.epoch = 0;
+    switch (a.dtype) {
+      case kF32: e = launch_f32(k, p, a.mode, s); break;
+      case kF16: e = launch_f16(k, p, a.mode, s); break;
+      default: e = launch_bf16(k, p, a.mode, s); break;
+    }
+  }
+  if (e != cudaSuccess) {
+    tl_last_cuda_error = e;
+    return GGRN_ERR_CUDA;
+  }
+  return GGRN_OK;
 }

@@ -63,7 +63,9 @@ typedef enum {
   GGRN_ERR_OVERLAP = 5,     /* the address range of out intersects that of y or gate */
   GGRN_ERR_CUDA = 6,        /* a CUDA runtime call (launch, query) failed */
   GGRN_ERR_UNSUPPORTED = 7, /* a forced path does not cover this shape */
-  GGRN_ERR_ARG = 8          /* an invalid path id, a NULL out-parameter, or a bad call list */
+  GGRN_ERR_ARG = 8,         /* an invalid path id, a NULL out-parameter, or a bad call list */
+  GGRN_ERR_LIMIT = 9        /* ggrn_forward_noalloc: more streamed units than
+                               GGRN_NOALLOC_MAX_UNITS */
 } ggrn_status;
 
 typedef enum { GGRN_F32 = 0, GGRN_F16 = 1, GGRN_BF16 = 2 } ggrn_dtype; /* T of y, gate, out */
@@ -199,6 +201,45 @@ int ggrn_fault_status(uint32_t* flags, int clear);
 /* Name of the CUDA error behind this thread's last GGRN_ERR_CUDA from a
  * launch ("cudaSuccess" if none); a static string, never NULL. */
 const char* ggrn_last_cuda_error(void);
+
+/*
+ * ggrn_forward_noalloc -- an addition of this library; the pages have no
+ * counterpart.
+ *
+ * For callers that cannot allocate device memory: code that runs while a
+ * framework's caching allocator owns the device (a raw cudaMalloc would fall
+ * outside its budget and accounting, or fail once the cache holds the free
+ * memory), real-time loops that must never block in the driver's allocator,
+ * and embedders whose device memory all comes from a pool they do not
+ * control.  This entry point runs the STREAM family with its dynamic unit
+ * schedule and keeps the schedule's claim counter in a fixed array built
+ * into the library: GGRN_NOALLOC_SCRATCH_BYTES per device, present on every
+ * GPU that loads the library until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.  (ggrn_forward
+ * allocates nothing either; this entry point differs in always taking the
+ * STREAM family and in keeping its schedule state in an array of its own
+ * that each call clears.)
+ *
+ * Arguments, layouts, ownership and numerics are those of ggrn_forward.
+ * Every call shares the array and clears the counter on `cuda_stream`
+ * before its kernel: calls of this entry point that overlap on the GPU
+ * (other streams, other threads) race on it and may leave outputs
+ * incomplete, so order them (one stream, or events).  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.
+ *
+ * Returns the ggrn_forward statuses, GGRN_ERR_UNSUPPORTED when the STREAM
+ * family cannot compute the shape (group bytes not a multiple of 8, or
+ * outside 4..128 shared-memory vectors per group), GGRN_ERR_ALIGN when the
+ * pointers or row strides are not 16-byte aligned, and GGRN_ERR_LIMIT when
+ * the call would stream more than GGRN_NOALLOC_MAX_UNITS units.
+ */
+#define GGRN_NOALLOC_SCRATCH_BYTES 256
+#define GGRN_NOALLOC_MAX_UNITS (1LL << 30)
+int ggrn_forward_noalloc(const void* y, const void* gate, const void* w, void* out,
+                         int64_t rows, int64_t width, int64_t group_size, int64_t y_row_stride,
+                         int64_t gate_row_stride, int64_t out_row_stride, float eps, int dtype,
+                         int mode, void* cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.ggrn_version() >= 100
-    for st in range(9):
+    for st in range(10):
         assert g.status_string(st)
     assert g.status_string(99) == "unknown status"
 
@@ -167,3 +167,27 @@ def test_binding_rejects_cpu_tensors():
     y = torch.zeros(2, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         g.forward(y, y, torch.ones(8), group_size=4, eps=1e-5)
+
+
+def test_noalloc_rejects_before_touching_the_device():
+    """The allocation-free entry point validates and plans on the host: bad
+    arguments, shapes its kernel family cannot stream, and calls beyond its
+    counter's limit return before any CUDA call."""
+    def call(**kw):
+        args = dict(y=Y, gate=GATE, w=W, out=OUT, rows=4, width=64, gs=32, ys=64, gts=64, os_=64,
+                    dtype=2, mode=0)
+        args.update(kw)
+        return g.ggrn_forward_noalloc(args["y"], args["gate"], args["w"], args["out"],
+                                      args["rows"], args["width"], args["gs"], args["ys"],
+                                      args["gts"], args["os_"], 1e-5, args["dtype"],
+                                      args["mode"], None)
+    assert call(rows=0, y=0, gate=0, w=0, out=0) == binding.OK
+    assert call(y=0) == binding.ERR_NULL
+    assert call(gs=3) == binding.ERR_SHAPE
+    assert call(y=Y + 2) == binding.ERR_ALIGN            # 2-byte aligned: no 16-byte vectors
+    assert call(width=64 * 12, gs=12, ys=64 * 12, gts=64 * 12, os_=64 * 12) == \
+        binding.ERR_UNSUPPORTED                          # 24-byte groups: not streamed
+    # 2^38 rows of one 32-wide group, 256 groups per unit: 2^30 units is the
+    # limit, 2^31 is beyond it (fake, far-apart addresses; nothing is read)
+    big = dict(y=1 << 46, gate=2 << 46, w=3 << 46, out=4 << 46, width=32, ys=32, gts=32, os_=32)
+    assert call(rows=1 << 39, **big) == binding.ERR_LIMIT

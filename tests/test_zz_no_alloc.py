@@ -1,0 +1,62 @@
+"""ggrn_forward_noalloc, the entry point for callers that cannot allocate
+device memory (a framework's caching allocator owns the device, a real-time
+loop must not block in the driver's allocator, or all device memory comes
+from a pool the caller does not control).
+
+It runs the streaming kernel with its unit-claim counter in a fixed array
+inside the library.  Two calls in a row through the C ABI must each give the
+output of the library's main entry point, ggrn_forward: the second call finds
+the first call's counter in the shared array and must clear it.
+
+The file is named to be collected last, so that a run stopping at the first
+failure has run every other test before this one.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import ggrn_inputs
+import gated_group_rmsnorm_gb300 as g
+from gated_group_rmsnorm_gb300 import binding
+from tests import gpu_util
+from tests.tolerance import ulp_dist
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.load()
+
+
+def _noalloc(dev, wl, out):
+    width = wl.width
+    rows, ys = binding._as_rows(dev.y, width, "y")
+    _, gts = binding._as_rows(dev.gate, width, "gate")
+    _, os_ = binding._as_rows(out, width, "out")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return g.ggrn_forward_noalloc(dev.y.data_ptr(), dev.gate.data_ptr(), dev.w.data_ptr(),
+                                  out.data_ptr(), rows, width, wl.group_size, ys, gts, os_,
+                                  ctypes.c_float(wl.eps), binding.DTYPE_CODE[wl.dtype], wl.mode,
+                                  stream)
+
+
+@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 1031), ("gdn_onnx", 2048),
+                                       ("strided_odd_span", 1900), ("mamba2_decode", 1)])
+def test_two_calls_match_the_main_entry_point(name, rows):
+    g.fault_status(clear=True)
+    wl = ggrn_inputs.WORKLOADS[name].with_rows(rows)
+    dev = gpu_util.to_device(ggrn_inputs.make_inputs(wl, seed=11))
+    ref = g.forward(dev.y, dev.gate, dev.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
+    outs = [torch.full_like(ref, -1280.0) for _ in range(2)]
+    for o in outs:
+        assert _noalloc(dev, wl, o) == binding.OK
+    torch.cuda.synchronize()
+    for o in outs:
+        # the tolerance of the parity tests (1 ulp of T); the same kernel
+        # family as the main entry point here, so in practice the same bits
+        assert int(ulp_dist(o.cpu(), ref.cpu()).max()) <= 1
+    assert g.fault_status() == 0
