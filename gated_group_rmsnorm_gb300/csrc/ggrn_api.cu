@@ -90,8 +90,7 @@ constexpr int kStraddleMaxVpl = 4;   // chunk of at most 128 vectors per warp
 constexpr int kStraddleBlock = 256;
 constexpr int kScalarBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;
-constexpr int kStreamWarps = 8;                 // consumer warps per CTA (target)
-constexpr int kStreamWarpsPaired = 12;          // ... for 4-lane x 7-vector paired items
+constexpr int kStreamWarps = 8;  // consumer warps per CTA (target)
 constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
 // Two CTAs per SM, 8 consumer warps, a double-buffered ring: the best of a
 // sweep over 1-2 CTAs/SM, 6-16 consumer warps and 2-4 stages on the prefill
@@ -390,13 +389,14 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   int target_warps = kStreamWarps;
   if (Q == 2 && nvec > 16 && nvec <= 28) {
     // a pair of 17..28 vectors (25 for the 100-wide bf16 odd span): 4 lanes x
-    // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25); more
-    // consumer warps carry the extra registers (measured best: 12)
+    // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25); as many
+    // consumer warps as the registers allow (one CTA per SM) hide the longer
+    // per-lane latency (odd span: 15 warps 6.42 TB/s, 12 warps 6.03)
     lanes = 4;
     vpl = 7;
-    target_warps = kStreamWarpsPaired;
+    target_warps = stream_max_warps(a.mode, vpl);
   }
-  const int wmax = vpl == 7 ? kStreamMaxWarps4x7 : kStreamMaxWarps;
+  const int wmax = stream_max_warps(a.mode, vpl);
   const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass
   const int64_t gpr = a.width / a.gs;
   const int64_t total = a.rows * gpr;

@@ -61,10 +61,14 @@ struct Plan {
   int ctas_per_sm = 0;
 };
 
-// Most consumer warps of a streaming launch (the kernels' launch bounds):
-// 4-lane x 7-vector paired items need more registers, hence fewer warps.
+// Most consumer warps of a streaming launch (the kernels' launch bounds).
+// 4-lane x 7-vector paired items fit 96 registers in MAMBA2 mode (16 warps);
+// in ONNX mode they also keep the gate's words, and 12 warps leave 128.
 constexpr int kStreamMaxWarps = 16;
-constexpr int kStreamMaxWarps4x7 = 12;
+constexpr int kStreamMaxWarps4x7Onnx = 12;
+constexpr int stream_max_warps(int mode, int vpl) {
+  return (vpl == 7 && mode == kOnnx) ? kStreamMaxWarps4x7Onnx : kStreamMaxWarps;
+}
 
 // Kernel parameters (passed by value).
 struct KParams {

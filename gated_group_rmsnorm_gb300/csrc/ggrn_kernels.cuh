@@ -199,6 +199,75 @@ __device__ __forceinline__ float silu(float b) {
   return (b * 0.0625f) * rcp_approx(d);
 }
 
+// ---------------------------------------------------------------------------
+// Packed f32 pairs.  sm_100-family SMs execute add/mul/fma on the two f32
+// halves of a 64-bit register pair in one instruction (PTX .f32x2), each
+// half rounded exactly as the scalar .rn instruction rounds it.  The
+// elementwise chain of the vector kernels runs on element pairs (2i, 2i+1),
+// halving its FMA-pipe instructions; MUFU operations stay scalar.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// (d0, d1) = (a0 * b0, a1 * b1)
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)));
+  upk2(r, d0, d1);
+}
+// (d0, d1) = (fma(a0, b0, c0), fma(a1, b1, c1))
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)), "l"(pk2(c0, c1)));
+  upk2(r, d0, d1);
+}
+
+// silu of two elements: the operations of silu<T>, on pairs.
+template <typename T>
+__device__ __forceinline__ void silu2(float b0, float b1, float& s0, float& s1) {
+  if (Elem<T>::kExactSilu) {
+    s0 = silu<T>(b0);
+    s1 = silu<T>(b1);
+    return;
+  }
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  float t0, t1, d0, d1, q0, q1;
+  mul2(t0, t1, b0, b1, kNegLog2e, kNegLog2e);
+  fma2(d0, d1, ex2_approx(t0), ex2_approx(t1), 0.0625f, 0.0625f, 0.0625f, 0.0625f);
+  mul2(q0, q1, b0, b1, 0.0625f, 0.0625f);
+  mul2(s0, s1, q0, q1, rcp_approx(d0), rcp_approx(d1));
+}
+
+// a[e] = y[e] * silu(g[e]), e < N (N even).
+template <typename T, int N>
+__device__ __forceinline__ void gated_vec(const float* y, const float* g, float* a) {
+#pragma unroll
+  for (int e = 0; e < N; e += 2) {
+    float s0, s1;
+    silu2<T>(g[e], g[e + 1], s0, s1);
+    mul2(a[e], a[e + 1], y[e], y[e + 1], s0, s1);
+  }
+}
+// s[e] = silu(g[e]), e < N (N even).
+template <typename T, int N>
+__device__ __forceinline__ void silu_vec(const float* g, float* s) {
+#pragma unroll
+  for (int e = 0; e < N; e += 2) silu2<T>(g[e], g[e + 1], s[e], s[e + 1]);
+}
+// (c0, c1) += squares of a[e], e < N (N even): even elements into c0, odd
+// into c1.
+template <int N>
+__device__ __forceinline__ void sumsq2(const float* a, float& c0, float& c1) {
+#pragma unroll
+  for (int e = 0; e < N; e += 2) fma2(c0, c1, a[e], a[e + 1], a[e], a[e + 1], c0, c1);
+}
+
 // floor(n / d) for the work-item counters (row = item / items_per_row).  The
 // host passes magic = floor(2^64 / d) + 1 when every n is below 2^32: then
 // n * magic / 2^64 exceeds n / d by less than 2^-32 <= 1/d, which cannot
@@ -217,18 +286,41 @@ __device__ __forceinline__ float normaliser(float m2, float gs_f, float eps) {
   return __frsqrt_rn(__fdiv_rn(m2, gs_f) + eps);
 }
 
+// Mamba-2 output values of N elements (N even), before the final rounding:
+// r = w * cast_T(gated * nf), with nf = nlo on the first N/2 elements and
+// nhi on the rest (the two groups of a vector split at its middle).
+template <typename T, int N>
+__device__ __forceinline__ void mamba2_out(const float* gated, float nlo, float nhi,
+                                           const float* w, float* r) {
+#pragma unroll
+  for (int e = 0; e < N; e += 2) {
+    const float nf = e < N / 2 ? nlo : nhi;
+    mul2(r[e], r[e + 1], gated[e], gated[e + 1], nf, nf);
+    Elem<T>::round_pair(r[e], r[e + 1]);
+    mul2(r[e], r[e + 1], w[e], w[e + 1], r[e], r[e + 1]);
+  }
+}
+
+// ONNX output values of N elements (N even): r = ((x * nf) * scale) * silu,
+// nf split as in mamba2_out.
+template <int N>
+__device__ __forceinline__ void onnx_out(const float* x, float nlo, float nhi, const float* sc,
+                                         const float* sg, float* r) {
+#pragma unroll
+  for (int e = 0; e < N; e += 2) {
+    const float nf = e < N / 2 ? nlo : nhi;
+    mul2(r[e], r[e + 1], x[e], x[e + 1], nf, nf);
+    mul2(r[e], r[e + 1], r[e], r[e + 1], sc[e], sc[e + 1]);
+    mul2(r[e], r[e + 1], r[e], r[e + 1], sg[e], sg[e + 1]);
+  }
+}
+
 // Mamba-2 epilogue on one vector: out = cast_T(w * cast_T(gated * nf)).
 template <typename T>
 __device__ __forceinline__ uint4 epilogue_mamba2(const float (&gated)[Elem<T>::E], float nf,
                                                  const float* wv) {
-  constexpr int E = Elem<T>::E;
-  float t[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) t[e] = gated[e] * nf;
-#pragma unroll
-  for (int e = 0; e < E; e += 2) Elem<T>::round_pair(t[e], t[e + 1]);
-#pragma unroll
-  for (int e = 0; e < E; ++e) t[e] = wv[e] * t[e];
+  float t[Elem<T>::E];
+  mamba2_out<T, Elem<T>::E>(gated, nf, nf, wv, t);
   return Elem<T>::pack(t);
 }
 
@@ -237,10 +329,8 @@ template <typename T>
 __device__ __forceinline__ uint4 epilogue_onnx(const float (&x)[Elem<T>::E],
                                                const float (&sg)[Elem<T>::E], float nf,
                                                const float (&sc)[Elem<T>::E]) {
-  constexpr int E = Elem<T>::E;
-  float r[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) r[e] = ((x[e] * nf) * sc[e]) * sg[e];
+  float r[Elem<T>::E];
+  onnx_out<Elem<T>::E>(x, nf, nf, sc, sg, r);
   return Elem<T>::pack(r);
 }
 
@@ -331,6 +421,7 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
     // the epilogue, so its raw bits wait there and silu is evaluated once.
     float a[VPL][E];
     float s0 = 0.0f, s1 = 0.0f;
+    float c0 = 0.0f, c1 = 0.0f;  // Q == 1: even / odd element partial sums
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
       float yf[E];
@@ -338,26 +429,24 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
       if (MODE == kMamba2) {
         float gf[E];
         Elem<T>::unpack(gr[k], gf);
-#pragma unroll
-        for (int e = 0; e < E; ++e) a[k][e] = yf[e] * silu<T>(gf[e]);
+        gated_vec<T, E>(yf, gf, a[k]);
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) a[k][e] = yf[e];
       }
       if constexpr (Q == 1) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) s0 = fmaf(a[k][e], a[k][e], s0);
+        sumsq2<E>(a[k], c0, c1);
       } else {
-        float h0 = 0.0f, h1 = 0.0f;
-#pragma unroll
-        for (int e = 0; e < E / 2; ++e) h0 = fmaf(a[k][e], a[k][e], h0);
-#pragma unroll
-        for (int e = E / 2; e < E; ++e) h1 = fmaf(a[k][e], a[k][e], h1);
+        float h0a = 0.0f, h0b = 0.0f, h1a = 0.0f, h1b = 0.0f;
+        sumsq2<E / 2>(a[k], h0a, h0b);
+        sumsq2<E / 2>(a[k] + E / 2, h1a, h1b);
+        const float h0 = h0a + h0b, h1 = h1a + h1b;
         const int v = k * LANES + lane;
         s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
         s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
       }
     }
+    if constexpr (Q == 1) s0 = c0 + c1;
 #pragma unroll
     for (int o = LANES / 2; o > 0; o >>= 1) {
       s0 += __shfl_xor_sync(0xffffffffu, s0, o);
@@ -379,12 +468,7 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
         if (MODE == kMamba2) {
           load_weight_vec<T, MODE>(p.w, col0 + (int64_t)v * E, wv);
           float t[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) t[e] = a[k][e] * (e < E / 2 ? nlo : nhi);
-#pragma unroll
-          for (int e = 0; e < E; e += 2) Elem<T>::round_pair(t[e], t[e + 1]);
-#pragma unroll
-          for (int e = 0; e < E; ++e) t[e] = wv[e] * t[e];
+          mamba2_out<T, E>(a[k], nlo, nhi, wv, t);
           o = Elem<T>::pack(t);
         } else {
           if constexpr (Q == 1) {
@@ -396,11 +480,10 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
             load_half_scale<T>(p.w, jlo, wv);
             load_half_scale<T>(p.w, jhi, wv + E / 2);
           }
-          float gf[E], r[E];
+          float gf[E], sg[E], r[E];
           Elem<T>::unpack(gr[k], gf);
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            r[e] = ((a[k][e] * (e < E / 2 ? nlo : nhi)) * wv[e]) * silu<T>(gf[e]);
+          silu_vec<T, E>(gf, sg);
+          onnx_out<E>(a[k], nlo, nhi, wv, sg, r);
           o = Elem<T>::pack(r);
         }
         st_stream(op + (int64_t)v * E, o);
@@ -447,23 +530,22 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParam
     }
     float a[VPL][E];
     float sg[MODE == kOnnx ? VPL : 1][E];
-    float ss = 0.0f;
+    float c0 = 0.0f, c1 = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
       float yf[E], gf[E];
       Elem<T>::unpack(yr[k], yf);
       Elem<T>::unpack(gr[k], gf);
+      if (MODE == kMamba2) {
+        gated_vec<T, E>(yf, gf, a[k]);
+      } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        if (MODE == kMamba2) {
-          a[k][e] = yf[e] * silu<T>(gf[e]);
-        } else {
-          a[k][e] = yf[e];
-          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
-        }
-        ss = fmaf(a[k][e], a[k][e], ss);
+        for (int e = 0; e < E; ++e) a[k][e] = yf[e];
+        silu_vec<T, E>(gf, sg[MODE == kOnnx ? k : 0]);
       }
+      sumsq2<E>(a[k], c0, c1);
     }
+    float ss = c0 + c1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
@@ -563,16 +645,15 @@ __global__ void __launch_bounds__(256, 3) k_straddle(const KParams p) {
       float sub[NS];
 #pragma unroll
       for (int i = 0; i < NS; ++i) sub[i] = 0.0f;
+      if (MODE == kMamba2) {
+        gated_vec<T, E>(yf, gf, a[k]);
+      } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        if (MODE == kMamba2) {
-          a[k][e] = yf[e] * silu<T>(gf[e]);
-        } else {
-          a[k][e] = yf[e];
-          sg[MODE == kOnnx ? k : 0][e] = silu<T>(gf[e]);
-        }
-        sub[e / G] = fmaf(a[k][e], a[k][e], sub[e / G]);
+        for (int e = 0; e < E; ++e) a[k][e] = yf[e];
+        silu_vec<T, E>(gf, sg[MODE == kOnnx ? k : 0]);
       }
+#pragma unroll
+      for (int e = 0; e < E; ++e) sub[e / G] = fmaf(a[k][e], a[k][e], sub[e / G]);
       float lo = 0.0f, hi = 0.0f;
 #pragma unroll
       for (int i = 0; i < NS; ++i) {
@@ -611,11 +692,11 @@ __global__ void __launch_bounds__(256, 3) k_straddle(const KParams p) {
           float wv[E];
           load_weight_vec<T, MODE>(p.w, c0 + e0, wv);
 #pragma unroll
-          for (int e = 0; e < E; ++e) r[e] = a[k][e] * nfv[e / G];
-#pragma unroll
-          for (int e = 0; e < E; e += 2) Elem<T>::round_pair(r[e], r[e + 1]);
-#pragma unroll
-          for (int e = 0; e < E; ++e) r[e] = wv[e] * r[e];
+          for (int e = 0; e < E; e += 2) {
+            mul2(r[e], r[e + 1], a[k][e], a[k][e + 1], nfv[e / G], nfv[(e + 1) / G]);
+            Elem<T>::round_pair(r[e], r[e + 1]);
+            mul2(r[e], r[e + 1], wv[e], wv[e + 1], r[e], r[e + 1]);
+          }
         } else {
           // scale index j of each element: offset from its group's start
           const int jlo = e0 - glo[k] * gs;

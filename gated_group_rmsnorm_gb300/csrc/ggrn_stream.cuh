@@ -159,15 +159,6 @@ __device__ __forceinline__ Words<NW> f32_to_words(const float* f) {
   return v;
 }
 
-// Round to T and widen back, element-wise (identity for f32).
-template <typename T, int N>
-__device__ __forceinline__ void round_to_t(float* f) {
-  if constexpr (sizeof(T) != 4) {
-#pragma unroll
-    for (int e = 0; e < N; e += 2) Elem<T>::round_pair(f[e], f[e + 1]);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Unit claims.  The claim word holds epoch << 32 | next: the launch whose
 // epoch (a number the host gives each launch) is installed hands out indices
@@ -436,9 +427,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
   const int nvec = static_cast<int>(Q * gs / SE);
   const int vb = static_cast<int>(gs / SE);
   const int items_per_pass = W * TPW;
-  for (int64_t i = 0;; ++i) {
-    const int s = static_cast<int>(i % NS);
-    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(i / NS) & 1u)) {
+  // stage s of the ring and the parity of its current fill
+  for (int s = 0, phase = 0;; s = (s + 1 == NS) ? 0 : s + 1, phase ^= (s == 0)) {
+    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(phase))) {
       if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
       break;
     }
@@ -471,6 +462,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
       }
       float a[VPL][SE];
       float s0 = 0.0f, s1 = 0.0f;
+      float c0 = 0.0f, c1 = 0.0f;  // Q == 1: even / odd element partial sums
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
         float yf[SE];
@@ -478,26 +470,24 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
         if (MODE == kMamba2) {
           float gf[SE];
           words_to_f32<T, NW>(gr[k], gf);
-#pragma unroll
-          for (int e = 0; e < SE; ++e) a[k][e] = yf[e] * silu<T>(gf[e]);
+          gated_vec<T, SE>(yf, gf, a[k]);
         } else {
 #pragma unroll
           for (int e = 0; e < SE; ++e) a[k][e] = yf[e];
         }
         if constexpr (Q == 1) {
-#pragma unroll
-          for (int e = 0; e < SE; ++e) s0 = fmaf(a[k][e], a[k][e], s0);
+          sumsq2<SE>(a[k], c0, c1);
         } else {
-          float h0 = 0.0f, h1 = 0.0f;
-#pragma unroll
-          for (int e = 0; e < SE / 2; ++e) h0 = fmaf(a[k][e], a[k][e], h0);
-#pragma unroll
-          for (int e = SE / 2; e < SE; ++e) h1 = fmaf(a[k][e], a[k][e], h1);
+          float h0a = 0.0f, h0b = 0.0f, h1a = 0.0f, h1b = 0.0f;
+          sumsq2<SE / 2>(a[k], h0a, h0b);
+          sumsq2<SE / 2>(a[k] + SE / 2, h1a, h1b);
+          const float h0 = h0a + h0b, h1 = h1a + h1b;
           const int v = k * L + tl;
           s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
           s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
         }
       }
+      if constexpr (Q == 1) s0 = c0 + c1;
 #pragma unroll
       for (int o = L / 2; o > 0; o >>= 1) {
         s0 += __shfl_xor_sync(0xffffffffu, s0, o);
@@ -518,11 +508,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
           if (MODE == kMamba2) {
             float wv[SE];
             load_w_cols<SE>(p, c, wcol + v * SE, wv);
-#pragma unroll
-            for (int e = 0; e < SE; ++e) r[e] = a[k][e] * (e < SE / 2 ? nlo : nhi);
-            round_to_t<T, SE>(r);
-#pragma unroll
-            for (int e = 0; e < SE; ++e) r[e] = wv[e] * r[e];
+            mamba2_out<T, SE>(a[k], nlo, nhi, wv, r);
           } else {
             float sc[SE], gf[SE];
             if constexpr (Q == 1) {
@@ -542,9 +528,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
                                       sc + SE / 2);
             }
             words_to_f32<T, NW>(gr[k], gf);
-#pragma unroll
-            for (int e = 0; e < SE; ++e)
-              r[e] = ((a[k][e] * (e < SE / 2 ? nlo : nhi)) * sc[e]) * silu<T>(gf[e]);
+            float sgv[SE];
+            silu_vec<T, SE>(gf, sgv);
+            onnx_out<SE>(a[k], nlo, nhi, sc, sgv, r);
           }
           stg_words<NW>(op + v * SE, f32_to_words<T, NW>(r));
         }
@@ -599,7 +585,7 @@ cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s) {
   if (p.smem_vec_bytes == 16 && p.items_groups == 2 && p.lanes == 4 && p.vpl == 7)
-    return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2, kStreamMaxWarps4x7>>(k, p, s);
+    return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2, stream_max_warps(MODE, 7)>>(k, p, s);
   if (p.vpl != 4) return cudaErrorInvalidConfiguration;
   if (p.smem_vec_bytes == 16 && p.items_groups == 1) return launch_stream_sv<T, MODE, 16, 1>(k, p, s);
   if (p.smem_vec_bytes == 16 && p.items_groups == 2) return launch_stream_sv<T, MODE, 16, 2>(k, p, s);

@@ -129,11 +129,11 @@ def test_plan_selects_families():
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
     # 9664: streamed in pairs of groups (25 whole 16-byte vectors) by teams of
-    # 4 lanes x 7 vectors; units of 4 whole rows (12 consumer warps x 8 teams
-    # x 2 groups = 192 groups), one CTA per SM
+    # 4 lanes x 7 vectors; units of 5 whole rows (15 consumer warps x 8 teams
+    # x 2 groups = 240 groups), one CTA per SM
     p = _plan(65536, 4800, 100, 2, ys=9664)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
-        (g.PATH_STREAM, 4, 7, 65536 // 4, 13 * 32, 152)
+        (g.PATH_STREAM, 4, 7, -(-65536 // 5), 16 * 32, 152)
     # register-resident teams of 8 lanes x 4 vectors, 24 pairs per row
     p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 8, 4, 24 * 65536)
