@@ -12,10 +12,11 @@ computed by hand-written CUDA kernels behind a C ABI (``include/ggrn.h``,
 """
 from .binding import (BF16, DTYPE_CODE, F16, F32, MAMBA2, ONNX, PATH_AUTO, PATH_NAMES,
                       PATH_SCALAR, PATH_STRADDLE, PATH_STREAM, PATH_TEAM, PATH_WIDE, DecodeGraph,
-                      GgrnError, fault_status, forward, ggrn_forward, ggrn_forward_noalloc,
-                      ggrn_forward_path, ggrn_plan, library_path, load, plan, status_string)
+                      GgrnError, fault_status, forward, forward_inproj, ggrn_forward,
+                      ggrn_forward_inproj, ggrn_forward_noalloc, ggrn_forward_path, ggrn_plan,
+                      library_path, load, plan, status_string)
 
-__all__ = ["forward", "plan", "DecodeGraph", "GgrnError", "ggrn_forward", "ggrn_forward_noalloc",
-           "ggrn_forward_path", "ggrn_plan", "load", "library_path", "status_string", "MAMBA2", "ONNX", "F32", "F16",
-           "BF16", "PATH_AUTO", "PATH_TEAM", "PATH_WIDE", "PATH_STRADDLE", "PATH_SCALAR",
+__all__ = ["forward", "forward_inproj", "plan", "DecodeGraph", "GgrnError", "ggrn_forward",
+           "ggrn_forward_inproj", "ggrn_forward_noalloc", "ggrn_forward_path", "ggrn_plan", "load",
+           "library_path", "status_string", "MAMBA2", "ONNX", "F32", "F16", "BF16", "PATH_AUTO", "PATH_TEAM", "PATH_WIDE", "PATH_STRADDLE", "PATH_SCALAR",
            "PATH_STREAM", "PATH_NAMES", "DTYPE_CODE", "fault_status"]

@@ -30,7 +30,8 @@ MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 # The exported symbols, as include/ggrn.h declares them.
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
-           "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc")
+           "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc",
+           "ggrn_forward_inproj")
 
 
 class GgrnError(RuntimeError):
@@ -85,6 +86,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
         L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
         L.ggrn_forward.restype = ci
+        L.ggrn_forward_inproj.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f, ci, ci,
+                                          vp]
+        L.ggrn_forward_inproj.restype = ci
         L.ggrn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci,
                                            ci, vp]
         L.ggrn_forward_noalloc.restype = ci
@@ -133,6 +137,13 @@ def ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride, gate_ro
                  out_row_stride, eps, dtype, mode, stream) -> int:
     return load().ggrn_forward(y, gate, w, out, rows, width, group_size, y_row_stride,
                                gate_row_stride, out_row_stride, eps, dtype, mode, stream)
+
+
+def ggrn_forward_inproj(inproj, inproj_row_stride, y_col, gate_col, w, out, out_row_stride, rows,
+                        width, group_size, eps, dtype, mode, stream) -> int:
+    return load().ggrn_forward_inproj(inproj, inproj_row_stride, y_col, gate_col, w, out,
+                                      out_row_stride, rows, width, group_size, eps, dtype, mode,
+                                      stream)
 
 
 def ggrn_forward_noalloc(y, gate, w, out, rows, width, group_size, y_row_stride,
@@ -227,14 +238,7 @@ def forward(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size:
         raise ValueError("gate must have the shape of y")
     if gate.dtype != y.dtype:
         raise ValueError("gate must have the dtype of y")
-    if m == MAMBA2 and (w.dtype != torch.float32 or w.numel() != width):
-        raise ValueError("MAMBA2 weight is float32 with `width` elements")
-    if m == ONNX:
-        if w.dtype != y.dtype or w.numel() != group_size:
-            raise ValueError("ONNX scale has the dtype of X and group_size elements")
-        w = w.reshape(-1)
-    if not w.is_contiguous():
-        w = w.contiguous()
+    w = _weight(w, m, width, group_size, y.dtype)
     if out is None:
         out = torch.empty(y.shape, dtype=y.dtype, device=y.device)
     elif out.shape != y.shape or out.dtype != y.dtype:
@@ -249,6 +253,49 @@ def forward(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size:
                            path, _stream_handle(y.device))
     if st != OK:
         raise GgrnError(st, "ggrn_forward")
+    return out
+
+
+def _weight(w: torch.Tensor, m: int, width: int, group_size: int, dtype) -> torch.Tensor:
+    if m == MAMBA2 and (w.dtype != torch.float32 or w.numel() != width):
+        raise ValueError("MAMBA2 weight is float32 with `width` elements")
+    if m == ONNX:
+        if w.dtype != dtype or w.numel() != group_size:
+            raise ValueError("ONNX scale has the dtype of X and group_size elements")
+        w = w.reshape(-1)
+    return w if w.is_contiguous() else w.contiguous()
+
+
+def forward_inproj(inproj: torch.Tensor, w: torch.Tensor, *, width: int, y_col: int,
+                   gate_col: int, group_size: int, eps: float, mode="mamba2",
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """The operation on y = inproj[..., y_col:y_col+width] and gate =
+    inproj[..., gate_col:gate_col+width], read in place from the packed
+    output of a fused input projection (``ggrn_forward_inproj``).
+
+    ``inproj``: [..., inproj_width] tensor of T with unit inner stride whose
+    leading axes fold into rows.  ``out``: optional [..., width] output
+    (allocated contiguous when omitted).
+    """
+    if not inproj.is_cuda:
+        raise ValueError("forward_inproj runs on CUDA tensors only (no CPU path)")
+    m = MODE_CODE[mode]
+    if inproj.dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {inproj.dtype}")
+    ipw = inproj.shape[-1]
+    rows, ips = _as_rows(inproj, ipw, "inproj")
+    w = _weight(w, m, width, group_size, inproj.dtype)
+    shape = tuple(inproj.shape[:-1]) + (width,)
+    if out is None:
+        out = torch.empty(shape, dtype=inproj.dtype, device=inproj.device)
+    elif tuple(out.shape) != shape or out.dtype != inproj.dtype:
+        raise ValueError("out must have the leading shape of inproj, width columns and its dtype")
+    _, os_ = _as_rows(out, width, "out")
+    st = ggrn_forward_inproj(inproj.data_ptr(), ips, y_col, gate_col, w.data_ptr(), out.data_ptr(),
+                             os_, rows, width, group_size, float(eps), DTYPE_CODE[inproj.dtype], m,
+                             _stream_handle(inproj.device))
+    if st != OK:
+        raise GgrnError(st, "ggrn_forward_inproj")
     return out
 
 

@@ -662,6 +662,26 @@ extern "C" int ggrn_forward_path(const void* y, const void* gate, const void* w,
   return forward_impl(a, path, static_cast<cudaStream_t>(cuda_stream));
 }
 
+extern "C" int ggrn_forward_inproj(const void* inproj, int64_t inproj_row_stride, int64_t y_col,
+                                   int64_t gate_col, const void* w, void* out,
+                                   int64_t out_row_stride, int64_t rows, int64_t width,
+                                   int64_t group_size, float eps, int dtype, int mode,
+                                   void* cuda_stream) {
+  if (rows < 0 || width <= 0) return GGRN_ERR_SHAPE;
+  if (rows == 0) return GGRN_OK;
+  if (!inproj) return GGRN_ERR_NULL;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GGRN_ERR_DTYPE;
+  // both column ranges inside a row of the packed buffer
+  if (y_col < 0 || gate_col < 0 || y_col > inproj_row_stride - width ||
+      gate_col > inproj_row_stride - width)
+    return GGRN_ERR_SHAPE;
+  const int es = elem_size(dtype);
+  const char* base = static_cast<const char*>(inproj);
+  const Args a = make_args(base + y_col * es, base + gate_col * es, w, out, rows, width, group_size,
+                           inproj_row_stride, inproj_row_stride, out_row_stride, eps, dtype, mode);
+  return forward_impl(a, kAuto, static_cast<cudaStream_t>(cuda_stream));
+}
+
 extern "C" int ggrn_plan(const void* y, const void* gate, const void* w, const void* out,
                          int64_t rows, int64_t width, int64_t group_size, int64_t y_row_stride,
                          int64_t gate_row_stride, int64_t out_row_stride, int dtype, int mode,

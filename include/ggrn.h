@@ -122,6 +122,29 @@ int ggrn_forward_path(const void* y, const void* gate, const void* w, void* out,
                       int64_t gate_row_stride, int64_t out_row_stride, float eps, int dtype,
                       int mode, int path, void* cuda_stream);
 
+/*
+ * ggrn_forward_inproj -- ggrn_forward reading y and gate straight from the
+ * packed output of a fused input projection ("gated_group_rmsnorm" page,
+ * Parallelization: a y/gate view split from the fused in-proj is read as
+ * it lies, with no host-side copy).
+ *   inproj            : const T*, rows of inproj_row_stride elements; y is
+ *                       columns [y_col, y_col + width) of every row and gate
+ *                       columns [gate_col, gate_col + width); other columns
+ *                       are never read.
+ *   inproj_row_stride : elements between rows (>= y_col + width and
+ *                       >= gate_col + width, also when rows == 1).
+ *   y_col, gate_col   : >= 0, in elements (any value: an offset that breaks
+ *                       16-byte alignment selects a narrower-load family).
+ *   w, out, out_row_stride, rows, width, group_size, eps, dtype, mode,
+ *   cuda_stream       : as in ggrn_forward.
+ * Returns the ggrn_forward statuses; GGRN_ERR_SHAPE also when a column range
+ * leaves the row.  out must not overlap the y or gate columns.
+ */
+int ggrn_forward_inproj(const void* inproj, int64_t inproj_row_stride, int64_t y_col,
+                        int64_t gate_col, const void* w, void* out, int64_t out_row_stride,
+                        int64_t rows, int64_t width, int64_t group_size, float eps, int dtype,
+                        int mode, void* cuda_stream);
+
 /* What a call would launch (host only: launches nothing, dereferences no pointer). */
 typedef struct {
   int32_t path;            /* ggrn_path chosen */

@@ -191,3 +191,26 @@ def test_noalloc_rejects_before_touching_the_device():
     # limit, 2^31 is beyond it (fake, far-apart addresses; nothing is read)
     big = dict(y=1 << 46, gate=2 << 46, w=3 << 46, out=4 << 46, width=32, ys=32, gts=32, os_=32)
     assert call(rows=1 << 39, **big) == binding.ERR_LIMIT
+
+
+def test_inproj_validation():
+    """The packed in-proj entry point checks its column ranges on the host."""
+    P = 0x1000000  # fake packed buffer; nothing is read
+
+    def call(**kw):
+        a = dict(inproj=P, stride=96, ycol=0, gcol=32, w=W, out=OUT, os_=32, rows=4, width=32,
+                 gs=8, dtype=2, mode=0)
+        a.update(kw)
+        return g.ggrn_forward_inproj(a["inproj"], a["stride"], a["ycol"], a["gcol"], a["w"],
+                                     a["out"], a["os_"], a["rows"], a["width"], a["gs"], 1e-5,
+                                     a["dtype"], a["mode"], None)
+    assert call(rows=0, inproj=0) == binding.OK
+    assert call(inproj=0) == binding.ERR_NULL
+    assert call(ycol=-1) == binding.ERR_SHAPE
+    assert call(ycol=65) == binding.ERR_SHAPE            # y columns leave the row
+    assert call(gcol=80) == binding.ERR_SHAPE            # gate columns leave the row
+    assert call(stride=48) == binding.ERR_SHAPE          # 32 + 32 > 48
+    assert call(gs=5) == binding.ERR_SHAPE               # width % group_size
+    assert call(dtype=7) == binding.ERR_DTYPE
+    assert call(out=P + 2 * 40) == binding.ERR_OVERLAP   # out inside the gate columns
+    assert call(w=0) == binding.ERR_NULL
