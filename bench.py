@@ -322,6 +322,63 @@ def _e2e(g, wl, steps: int, device) -> dict:
             "ms_per_step": round(ms / steps, 4)}
 
 
+def unfused_chain_fn(wl):
+    """Context, not a product path: the operation as separate PyTorch ops on
+    the GPU, the multi-dispatch chain a fused kernel replaces (widen, y *
+    silu(gate), per-group mean of squares and rsqrt, normalise and cast,
+    weight and cast; ONNX: the normalised X times scale and silu(gate))."""
+    import torch.nn.functional as F
+    rows, width, gs = wl.rows, wl.width, wl.group_size
+
+    def chain(inp):
+        yf, gf = inp.y.float(), inp.gate.float()
+        if wl.mode == 0:
+            gated = (yf * F.silu(gf)).view(rows, width // gs, gs)
+            nf = torch.rsqrt(gated.pow(2).mean(-1, keepdim=True) + wl.eps)
+            t = (gated * nf).to(wl.dtype).view(rows, width)
+            return (inp.w * t.float()).to(wl.dtype)
+        x = yf.view(rows, width // gs, gs)
+        nf = torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + wl.eps)
+        r = (x * nf).view(rows, width) * inp.w.float().repeat(width // gs) * F.silu(gf)
+        return r.to(wl.dtype)
+    return chain
+
+
+def _unfused_chain(wl, sets, steps: int) -> dict:
+    """The unfused chain timed like the fused launch, on the same rotating inputs."""
+    chain = unfused_chain_fn(wl)
+    for i in range(3):
+        chain(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    ops = None
+    try:  # dispatched ATen ops that are not views: one GPU kernel each here
+        from torch.utils._python_dispatch import TorchDispatchMode
+
+        class _Count(TorchDispatchMode):
+            n = 0
+
+            def __torch_dispatch__(self, func, types, args=(), kwargs=None):
+                if not getattr(func, "is_view", False):
+                    _Count.n += 1
+                return func(*args, **(kwargs or {}))
+        with _Count():
+            chain(sets[0])
+        ops = _Count.n
+    except Exception:  # the count is optional context
+        ops = None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        chain(sets[i % len(sets)])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(wl.algorithmic_bytes() / (ms / 1e3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps, "aten_ops_per_step": ops,
+            "note": "the operation as separate PyTorch GPU ops (unfused chain), same "
+                    "algorithmic bytes and inputs; context for the single fused launch"}
+
+
 def run_ours(args) -> None:
     rank, world, local_rank = dist_env()
     import torch.distributed as dist
@@ -385,6 +442,8 @@ def run_ours(args) -> None:
         e2e["value"] = round(world * bytes_per_step / (e2e_ms / 1e3) / 1e9, 2)
         e2e["ms_per_step"] = round(e2e_ms, 4)
     decode = _decode_numbers(g, device) if (rank == 0 and not args.no_decode) else None
+    if rank == 0 and world == 1 and not args.no_unfused:
+        extra["unfused_chain"] = _unfused_chain(wl, sets, min(args.steps, 200))
 
     if rank != 0:
         return
@@ -566,6 +625,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip timing the unfused PyTorch op chain (context)")
     ap.add_argument("--rows-sweep", default="",
                     help="comma-separated row counts: time per launch vs rows, and the fit "
                          "(fixed cost, steady-state GB/s); not the benchmark line")
