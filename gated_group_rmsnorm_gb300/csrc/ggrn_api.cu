@@ -92,9 +92,7 @@ constexpr int kScalarBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;
 constexpr int kStreamWarps = 8;  // consumer warps per CTA (target)
 constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
-// Two CTAs per SM, 8 consumer warps, a double-buffered ring: the best of a
-// sweep over 1-2 CTAs/SM, 6-16 consumer warps and 2-4 stages on the prefill
-// and gated-DeltaNet shapes (deeper rings were up to 5% slower).
+// Ring stages (at most; the shared-memory budget may allow fewer).
 constexpr int64_t kStreamMaxStages = 2;
 constexpr int64_t kStreamMaxWeightBytes = 64 * 1024;
 
@@ -386,7 +384,21 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   if (nvec < 4 || nvec > 128) return GGRN_ERR_UNSUPPORTED;
   int lanes = next_pow2(static_cast<int>(ceil_div(nvec, 4)));
   int vpl = 4;
+  // Consumer warps and ring depth by team width, from a sweep of 4-16 warps,
+  // 1-2 CTAs per SM and 2-4 stages over groups of 64..960 elements (claimed
+  // units): one group per warp (32-lane teams) runs best with 16 warps and
+  // three stages in one CTA per SM (+0.7 % at 960); narrow groups (teams of
+  // at most 4 lanes) with 6 warps and three stages, two CTAs per SM (+1.5 to
+  // 1.9 % at 64 and 128); 8- and 16-lane teams with 8 warps and two stages.
   int target_warps = kStreamWarps;
+  int64_t max_stages = kStreamMaxStages;
+  if (Q == 1 && lanes == 32) {
+    target_warps = 16;
+    max_stages = 3;
+  } else if (Q == 1 && lanes <= 4) {
+    target_warps = 6;
+    max_stages = 3;
+  }
   if (Q == 2 && nvec > 16 && nvec <= 28) {
     // a pair of 17..28 vectors (25 for the 100-wide bf16 odd span): 4 lanes x
     // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25); as many
@@ -441,7 +453,7 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   const int64_t wb = a.mode == kMamba2 ? a.width * 4 : a.gs * es;
   int cps, ns;
   int64_t wstage;
-  if (!stream_smem(stage_bytes, wb, kStreamMaxStages, &cps, &ns, &wstage))
+  if (!stream_smem(stage_bytes, wb, max_stages, &cps, &ns, &wstage))
     return GGRN_ERR_UNSUPPORTED;
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
   if (!forced && units < 2 * gmax) return GGRN_ERR_UNSUPPORTED;

@@ -108,20 +108,22 @@ def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
 
 
 def test_plan_selects_families():
-    # Mamba-2 prefill 4096x7680, group 960: streamed, one row (8 groups) per
-    # unit, one warp per group (32 lanes x 4 vectors of 16 bytes), 8 consumer
-    # warps + 1 producer warp, 2 CTAs on each of 152 SMs claiming units
+    # Mamba-2 prefill 4096x7680, group 960: streamed, two rows (16 groups) per
+    # unit, one warp per group (32 lanes x 4 vectors of 16 bytes), 16 consumer
+    # warps + 1 producer warp, one CTA on each of 152 SMs claiming units
     p = _plan(4096, 7680, 960, 2)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads) == \
-        (g.PATH_STREAM, 32, 4, 4096, 288)
-    assert p.grid_blocks == 2 * 152
+        (g.PATH_STREAM, 32, 4, 2048, 17 * 32)
+    assert p.grid_blocks == 152
     # the same shape on the register-resident family: one warp per group
     p = _plan(4096, 7680, 960, 2, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
     # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 4-lane teams with 4
-    # vectors each, 8 groups per warp; streamed in units of 64 groups (2 rows)
+    # vectors each, 8 groups per warp; 6 consumer warps, units of 48 groups
+    # of the contiguous rows (the last one partial), 2 CTAs per SM
     p = _plan(32768, 4096, 128, 1, mode=1)
-    assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_STREAM, 4, 4, 16384)
+    assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
+        (g.PATH_STREAM, 4, 4, -(-32768 * 32 // 48), 7 * 32, 304)
     p = _plan(32768, 4096, 128, 1, mode=1, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 4)
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
