@@ -378,8 +378,12 @@ __device__ __forceinline__ void load_half_scale(const void* w, int64_t j, float*
 // LANES consecutive vectors.  Teams are aligned LANES-lane segments of a
 // warp; the xor butterfly with offsets < LANES never crosses a segment.
 // ---------------------------------------------------------------------------
+// Resident CTAs per SM the register budget targets: ONNX keeps the gate's
+// raw words until the epilogue, so its kernels get a larger budget.
+constexpr int team_min_blocks(int mode) { return mode == kOnnx ? 3 : 4; }
+
 template <typename T, int MODE, int LANES, int VPL, int Q>
-__global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
+__global__ void __launch_bounds__(256, team_min_blocks(MODE)) k_team(const KParams p) {
   constexpr int E = Elem<T>::E;
   pdl_wait();
   pdl_launch_dependents();
@@ -499,7 +503,8 @@ __global__ void __launch_bounds__(256, 4) k_team(const KParams p) {
 // every thread adds them in the same order.
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, int VPL, int MAXT>
-__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParams p) {
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? (MODE == kOnnx ? 4 : 5) : 1)
+    k_wide(const KParams p) {
   constexpr int E = Elem<T>::E;
   __shared__ float red[2][32];
   pdl_wait();
@@ -528,20 +533,21 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParam
         gr[k] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // MAMBA2: a = gated.  ONNX: a = x; the gate's raw words wait for the
+    // epilogue (fewer live registers than its widened silu).
     float a[VPL][E];
-    float sg[MODE == kOnnx ? VPL : 1][E];
     float c0 = 0.0f, c1 = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      float yf[E], gf[E];
+      float yf[E];
       Elem<T>::unpack(yr[k], yf);
-      Elem<T>::unpack(gr[k], gf);
       if (MODE == kMamba2) {
+        float gf[E];
+        Elem<T>::unpack(gr[k], gf);
         gated_vec<T, E>(yf, gf, a[k]);
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) a[k][e] = yf[e];
-        silu_vec<T, E>(gf, sg[MODE == kOnnx ? k : 0]);
       }
       sumsq2<E>(a[k], c0, c1);
     }
@@ -566,7 +572,10 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParam
           o = epilogue_mamba2<T>(a[k], nf, wv);
         } else {
           load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
-          o = epilogue_onnx<T>(a[k], sg[MODE == kOnnx ? k : 0], nf, wv);
+          float gf[E], sg[E];
+          Elem<T>::unpack(gr[k], gf);
+          silu_vec<T, E>(gf, sg);
+          o = epilogue_onnx<T>(a[k], sg, nf, wv);
         }
         st_stream(op + (int64_t)v * E, o);
       }
@@ -587,7 +596,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 5 : 1) k_wide(const KParam
 // part_hi[32*VPL], nf[chunk_groups]; no block-wide barrier.
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, int VPL, int G>
-__global__ void __launch_bounds__(256, 3) k_straddle(const KParams p) {
+__global__ void __launch_bounds__(256, MODE == kOnnx ? 2 : 3) k_straddle(const KParams p) {
   constexpr int E = Elem<T>::E;
   constexpr int NS = E / G;          // sub-blocks per vector
   constexpr int SLOTS = 32 * VPL;
