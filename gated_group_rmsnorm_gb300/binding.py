@@ -31,7 +31,7 @@ MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
            "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc",
-           "ggrn_forward_inproj")
+           "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_host_workspace_bytes")
 
 
 class GgrnError(RuntimeError):
@@ -86,6 +86,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
         L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
         L.ggrn_forward.restype = ci
+        L.ggrn_forward_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci,
+                                        vp, i64, vp]
+        L.ggrn_forward_host.restype = ci
+        L.ggrn_host_workspace_bytes.argtypes = [i64, i64, ci]
+        L.ggrn_host_workspace_bytes.restype = i64
         L.ggrn_forward_inproj.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f, ci, ci,
                                           vp]
         L.ggrn_forward_inproj.restype = ci
@@ -144,6 +149,13 @@ def ggrn_forward_inproj(inproj, inproj_row_stride, y_col, gate_col, w, out, out_
     return load().ggrn_forward_inproj(inproj, inproj_row_stride, y_col, gate_col, w, out,
                                       out_row_stride, rows, width, group_size, eps, dtype, mode,
                                       stream)
+
+
+def ggrn_forward_host(y, gate, w, out, rows, width, group_size, y_row_stride, gate_row_stride,
+                      out_row_stride, eps, dtype, mode, workspace, workspace_bytes, stream) -> int:
+    return load().ggrn_forward_host(y, gate, w, out, rows, width, group_size, y_row_stride,
+                                    gate_row_stride, out_row_stride, eps, dtype, mode, workspace,
+                                    workspace_bytes, stream)
 
 
 def ggrn_forward_noalloc(y, gate, w, out, rows, width, group_size, y_row_stride,
@@ -296,6 +308,54 @@ def forward_inproj(inproj: torch.Tensor, w: torch.Tensor, *, width: int, y_col: 
                              _stream_handle(inproj.device))
     if st != OK:
         raise GgrnError(st, "ggrn_forward_inproj")
+    return out
+
+
+def host_workspace(rows: int, width: int, dtype, device) -> torch.Tensor:
+    """A device workspace of the size ggrn_forward_host wants for full chunks."""
+    n = load().ggrn_host_workspace_bytes(rows, width, DTYPE_CODE[dtype])
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def forward_host(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size: int,
+                 eps: float, mode="mamba2", out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """The operation on CPU tensors, copies and kernels overlapped
+    (``ggrn_forward_host``), enqueued on the current stream of ``w``'s device.
+
+    ``y``, ``gate``: CPU [..., width] tensors (pinned for the copies to
+    overlap).  ``w``: the weight / scale on the GPU.  ``out``: optional CPU
+    output (allocated pinned when omitted).  ``workspace``: optional device
+    uint8 tensor (``host_workspace`` when omitted).  The result is complete
+    when the stream reaches this point (synchronise before reading it).
+    """
+    if y.is_cuda or gate.is_cuda:
+        raise ValueError("forward_host takes y and gate in host memory")
+    if not w.is_cuda:
+        raise ValueError("the weight lives on the GPU")
+    m = MODE_CODE[mode]
+    width = y.shape[-1]
+    if gate.shape != y.shape or gate.dtype != y.dtype:
+        raise ValueError("gate must have the shape and dtype of y")
+    if y.dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {y.dtype}")
+    w = _weight(w, m, width, group_size, y.dtype)
+    if out is None:
+        out = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    elif out.is_cuda or out.shape != y.shape or out.dtype != y.dtype:
+        raise ValueError("out must be a host tensor with the shape and dtype of y")
+    rows, ys = _as_rows(y, width, "y")
+    _, gts = _as_rows(gate, width, "gate")
+    _, os_ = _as_rows(out, width, "out")
+    if workspace is None:
+        workspace = host_workspace(rows, width, y.dtype, w.device)
+    with torch.cuda.device(w.device):
+        st = ggrn_forward_host(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows,
+                               width, group_size, ys, gts, os_, float(eps), DTYPE_CODE[y.dtype], m,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(w.device))
+    if st != OK:
+        raise GgrnError(st, "ggrn_forward_host")
     return out
 
 

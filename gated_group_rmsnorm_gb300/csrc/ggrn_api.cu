@@ -608,6 +608,18 @@ struct DecodeGraph {
 
 }  // namespace
 
+Args call_args(const void* y, const void* gate, const void* w, void* out, int64_t rows,
+                int64_t width, int64_t gs, int64_t ys, int64_t gts, int64_t os, float eps,
+                int dtype, int mode) {
+  return make_args(y, gate, w, out, rows, width, gs, ys, gts, os, eps, dtype, mode);
+}
+
+int validate_call(const Args& a) { return validate(a); }
+
+int forward_call(const Args& a, cudaStream_t s) { return forward_impl(a, kAuto, s); }
+
+void record_cuda_error(cudaError_t e) { tl_last_cuda_error = e; }
+
 KParams make_params(const Args& a, const Plan& p) {
   KParams k;
   k.y = a.y;

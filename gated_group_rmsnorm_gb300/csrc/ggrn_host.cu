@@ -1,0 +1,175 @@
+// ggrn_host.cu -- ggrn_forward_host: the operation on host-resident y, gate
+// and out, with the host<->device copies overlapped with the kernels.
+//
+// Rows are cut into chunks that cycle through kSlots slots of a caller-owned
+// device workspace (y, gate and out of one chunk per slot).  Three streams of
+// the library run, for consecutive chunks at the same time, the host-to-
+// device copies of chunk i, the kernel of chunk i-1 and the device-to-host
+// copy of chunk i-2; events order each chunk's three steps and keep a slot
+// from being refilled before its output has left.  With pinned host memory
+// the two copy directions share the link at once, so a call takes about the
+// time of its bytes at the combined host-device rate instead of the sum of
+// both directions' times.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/ggrn.h"
+#include "ggrn_internal.h"
+
+namespace ggrn {
+namespace {
+
+constexpr int kSlots = 3;
+// y + gate bytes per chunk aimed at: small enough for ~8+ chunks at the
+// benchmark sizes (good overlap), large enough that a chunk's kernel is a
+// few microseconds against tens of microseconds of copies.
+constexpr int64_t kChunkTargetBytes = int64_t{8} << 20;
+constexpr int64_t kAlign = 256;
+
+int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int es_of(int dtype) { return dtype == kF32 ? 4 : 2; }
+
+int64_t target_chunk_rows(int64_t rows, int64_t width, int es) {
+  const int64_t r = std::max<int64_t>(1, kChunkTargetBytes / (2 * width * es));
+  return std::min(rows, r);
+}
+
+// Streams and events of one device, created once (the first call there) and
+// shared by all calls on that device; `mu` keeps one call's enqueue
+// sequence whole when several host threads call at once.
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in[kSlots] = {}, done[kSlots] = {}, freed[kSlots] = {};
+};
+
+HostPipe* pipe_for_device(int dev) {
+  static HostPipe pipes[64];
+  return (dev >= 0 && dev < 64) ? &pipes[dev] : nullptr;
+}
+
+cudaError_t pipe_init(HostPipe* hp) {
+  if (hp->ready) return cudaSuccess;
+  cudaError_t e;
+  for (cudaStream_t* st : {&hp->h2d, &hp->comp, &hp->d2h})
+    if ((e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  cudaEvent_t* evs[] = {&hp->start, &hp->end};
+  for (cudaEvent_t* ev : evs)
+    if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  for (int i = 0; i < kSlots; ++i)
+    for (cudaEvent_t* ev : {&hp->in[i], &hp->done[i], &hp->freed[i]})
+      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  hp->ready = true;
+  return cudaSuccess;
+}
+
+// Copy `n` rows of `width` elements between a strided host matrix and a
+// contiguous device block (one 1-D copy when the host rows are contiguous).
+cudaError_t copy_rows(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch,
+                      int64_t row_bytes, int64_t n, cudaMemcpyKind kind, cudaStream_t s) {
+  if (dst_pitch == row_bytes && src_pitch == row_bytes)
+    return cudaMemcpyAsync(dst, src, static_cast<size_t>(n * row_bytes), kind, s);
+  return cudaMemcpy2DAsync(dst, static_cast<size_t>(dst_pitch), src, static_cast<size_t>(src_pitch),
+                           static_cast<size_t>(row_bytes), static_cast<size_t>(n), kind, s);
+}
+
+}  // namespace
+}  // namespace ggrn
+
+using namespace ggrn;
+
+extern "C" int64_t ggrn_host_workspace_bytes(int64_t rows, int64_t width, int dtype) {
+  if (rows <= 0 || width <= 0) return 0;
+  const int es = es_of(dtype);
+  return kSlots * 3 * align_up(target_chunk_rows(rows, width, es) * width * es);
+}
+
+extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w,
+                                 void* out_host, int64_t rows, int64_t width,
+                                 int64_t group_size, int64_t y_row_stride,
+                                 int64_t gate_row_stride, int64_t out_row_stride, float eps,
+                                 int dtype, int mode, void* workspace, int64_t workspace_bytes,
+                                 void* cuda_stream) {
+  // The host matrices get the checks of ggrn_forward (shapes, dtype, NULL,
+  // element alignment, out overlapping y or gate).
+  const Args a = call_args(y_host, gate_host, w, out_host, rows, width, group_size, y_row_stride,
+                           gate_row_stride, out_row_stride, eps, dtype, mode);
+  int st = validate_call(a);
+  if (st != GGRN_OK || rows == 0) return st;
+  if (!workspace) return GGRN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return GGRN_ERR_ALIGN;
+  const int es = es_of(dtype);
+  const int64_t row_bytes = width * es;
+  // rows per chunk: the target, as far as kSlots x (y, gate, out) slots of
+  // 256-byte-aligned parts fit
+  int64_t chunk = std::min(target_chunk_rows(rows, width, es),
+                           workspace_bytes / (kSlots * 3 * row_bytes));
+  while (chunk > 0 && kSlots * 3 * align_up(chunk * row_bytes) > workspace_bytes) --chunk;
+  if (chunk < 1) return GGRN_ERR_ARG;
+  const int64_t part = align_up(chunk * row_bytes);  // one tensor of one slot
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  HostPipe* hp = e == cudaSuccess ? pipe_for_device(dev) : nullptr;
+  if (!hp) {
+    record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return GGRN_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(hp->mu);
+  if ((e = pipe_init(hp)) != cudaSuccess) {
+    record_cuda_error(e);
+    return GGRN_ERR_CUDA;
+  }
+  const cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
+  // everything enqueued so far on the caller's stream comes first
+  e = cudaEventRecord(hp->start, caller);
+  for (cudaStream_t s : {hp->h2d, hp->comp, hp->d2h})
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->start, 0);
+  const char* yh = static_cast<const char*>(y_host);
+  const char* gh = static_cast<const char*>(gate_host);
+  char* oh = static_cast<char*>(out_host);
+  char* ws = static_cast<char*>(workspace);
+  const int64_t ysb = a.ys * es, gsb = a.gts * es, osb = a.os * es;
+  for (int64_t r0 = 0, c = 0; r0 < rows && e == cudaSuccess && st == GGRN_OK; r0 += chunk, ++c) {
+    const int64_t n = std::min(chunk, rows - r0);
+    const int slot = static_cast<int>(c % kSlots);
+    char* dy = ws + slot * 3 * part;
+    char* dg = dy + part;
+    char* dout = dg + part;
+    // host -> device, once the slot's previous output has left
+    e = cudaStreamWaitEvent(hp->h2d, hp->freed[slot], 0);
+    if (e == cudaSuccess)
+      e = copy_rows(dy, row_bytes, yh + r0 * ysb, ysb, row_bytes, n, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess)
+      e = copy_rows(dg, row_bytes, gh + r0 * gsb, gsb, row_bytes, n, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in[slot], hp->h2d);
+    // the kernel on the chunk (contiguous rows in the slot)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in[slot], 0);
+    if (e == cudaSuccess) {
+      st = forward_call(call_args(dy, dg, w, dout, n, width, group_size, width, width, width, eps,
+                                  dtype, mode),
+                        hp->comp);
+      if (st == GGRN_OK) e = cudaEventRecord(hp->done[slot], hp->comp);
+    }
+    // device -> host
+    if (e == cudaSuccess && st == GGRN_OK) e = cudaStreamWaitEvent(hp->d2h, hp->done[slot], 0);
+    if (e == cudaSuccess && st == GGRN_OK)
+      e = copy_rows(oh + r0 * osb, osb, dout, row_bytes, row_bytes, n, cudaMemcpyDeviceToHost,
+                    hp->d2h);
+    if (e == cudaSuccess && st == GGRN_OK) e = cudaEventRecord(hp->freed[slot], hp->d2h);
+  }
+  // the caller's stream continues after the last output has arrived (the
+  // last copy follows every kernel and every input copy of the call)
+  if (e == cudaSuccess && st == GGRN_OK) e = cudaEventRecord(hp->end, hp->d2h);
+  if (e == cudaSuccess && st == GGRN_OK) e = cudaStreamWaitEvent(caller, hp->end, 0);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return GGRN_ERR_CUDA;
+  }
+  return st;
+}

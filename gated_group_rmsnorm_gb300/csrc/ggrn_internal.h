@@ -110,6 +110,17 @@ struct KParams {
 
 KParams make_params(const Args& a, const Plan& p);
 
+// The ggrn_forward path for other translation units of the library: the
+// arguments of one call (a single row has no row stride), their checks, and
+// validation + automatic selection + launch on a stream.
+Args call_args(const void* y, const void* gate, const void* w, void* out, int64_t rows,
+               int64_t width, int64_t gs, int64_t ys, int64_t gts, int64_t os, float eps,
+               int dtype, int mode);
+int validate_call(const Args& a);
+int forward_call(const Args& a, cudaStream_t s);
+// Remember the CUDA error behind a GGRN_ERR_CUDA (ggrn_last_cuda_error).
+void record_cuda_error(cudaError_t e);
+
 // Launchers, one per element type (defined in ggrn_kernels_<T>.cu).  They
 // enqueue the kernel the plan names with programmatic dependent launch
 // allowed, and return the CUDA error of the launch.

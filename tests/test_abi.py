@@ -216,3 +216,27 @@ def test_inproj_validation():
     assert call(dtype=7) == binding.ERR_DTYPE
     assert call(out=P + 2 * 40) == binding.ERR_OVERLAP   # out inside the gate columns
     assert call(w=0) == binding.ERR_NULL
+
+
+def test_host_pipeline_rejects_before_enqueueing():
+    """ggrn_forward_host checks the host matrices and the workspace first."""
+    H_Y, H_G, H_O = 0x10000000, 0x20000000, 0x30000000  # fake host addresses
+
+    def call(**kw):
+        a = dict(y=H_Y, gate=H_G, w=W, out=H_O, rows=4, width=64, gs=32, ws=0x40000000,
+                 wsb=1 << 20, dtype=2)
+        a.update(kw)
+        return g.ggrn_forward_host(a["y"], a["gate"], a["w"], a["out"], a["rows"], a["width"],
+                                   a["gs"], a["width"], a["width"], a["width"], 1e-5, a["dtype"], 0,
+                                   a["ws"], a["wsb"], None)
+    assert call(rows=0, y=0, gate=0, out=0, ws=0) == binding.OK
+    assert call(y=0) == binding.ERR_NULL
+    assert call(gs=5) == binding.ERR_SHAPE
+    assert call(out=H_Y + 64) == binding.ERR_OVERLAP
+    assert call(ws=0) == binding.ERR_NULL
+    assert call(ws=0x40000008) == binding.ERR_ALIGN
+    assert call(wsb=1000) == binding.ERR_ARG       # not one row per slot
+    lib = g.load()
+    need = lib.ggrn_host_workspace_bytes(4096, 7680, 2)
+    assert need == 3 * 3 * (-(-min(4096, (8 << 20) // (2 * 7680 * 2)) * 7680 * 2 // 256) * 256)
+    assert lib.ggrn_host_workspace_bytes(0, 7680, 2) == 0

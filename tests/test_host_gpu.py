@@ -1,0 +1,80 @@
+"""ggrn_forward_host: host-resident y, gate and out, the copies overlapped
+with the kernels (GPU).  Every output row must arrive, match the oracle,
+and match the device-resident call within the parity tolerance (chunks may
+take another kernel family than the whole call)."""
+import pytest
+import torch
+
+import ggrn_inputs
+import gated_group_rmsnorm_gb300 as g
+from tests import gpu_util
+from tests.tolerance import ulp_dist
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.load()
+
+
+def _host_case(name, rows, pinned=True, seed=0):
+    wl = ggrn_inputs.WORKLOADS[name].with_rows(rows)
+    inp = ggrn_inputs.make_inputs(wl, seed=seed)
+    if inp.packed is not None:
+        packed = inp.packed.pin_memory() if pinned else inp.packed.clone()
+        y, gate = packed[:, :wl.width], packed[:, wl.width:2 * wl.width]
+    else:
+        y = inp.y.pin_memory() if pinned else inp.y.clone()
+        gate = inp.gate.pin_memory() if pinned else inp.gate.clone()
+    return wl, inp, y, gate
+
+
+@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 1031), ("gdn_onnx", 2048),
+                                       ("strided_odd_span", 777), ("wide_single_group", 300),
+                                       ("mamba2_decode", 1)])
+def test_matches_oracle_and_device_call(name, rows):
+    wl, inp, y, gate = _host_case(name, rows)
+    w = inp.w.cuda()
+    out = g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
+    torch.cuda.synchronize()
+    assert not out.is_cuda
+    res = gpu_util.compare(out, inp, wl.group_size, wl.eps, wl.mode)
+    assert res["ok"], res
+    dev = g.forward(y.cuda(), gate.cuda(), w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
+    assert int(ulp_dist(out, dev.cpu()).max()) <= 1
+
+
+def test_small_workspace_pageable_memory_and_reuse():
+    """One row per slot (hundreds of chunks), pageable host memory, and the
+    same workspace for two calls in a row."""
+    wl, inp, y, gate = _host_case("mamba2_prefill", 200, pinned=False, seed=4)
+    w = inp.w.cuda()
+    ws = torch.empty(3 * 3 * wl.width * 2 + 2304, dtype=torch.uint8, device="cuda")
+    outs = [g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps, workspace=ws)
+            for _ in range(2)]
+    torch.cuda.synchronize()
+    for o in outs:
+        res = gpu_util.compare(o, inp, wl.group_size, wl.eps, wl.mode)
+        assert res["ok"], res
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_ordered_on_the_callers_stream():
+    """Work enqueued on the caller's stream afterwards sees every output row:
+    a device copy of the host output, made on a side stream after the call,
+    equals the output read after a full synchronisation."""
+    wl, inp, y, gate = _host_case("gdn_onnx", 1500, seed=6)
+    w = inp.w.cuda()
+    side = torch.cuda.Stream()
+    out = torch.full(y.shape, -1280.0, dtype=y.dtype).pin_memory()
+    back = torch.empty(y.shape, dtype=y.dtype, device="cuda")
+    with torch.cuda.stream(side):
+        g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode, out=out)
+        back.copy_(out, non_blocking=True)   # ordered after the call on `side`
+    side.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(back.cpu().view(torch.int16), out.view(torch.int16))
+    assert not bool((out == -1280.0).any())
