@@ -23,10 +23,12 @@ namespace ggrn {
 namespace {
 
 constexpr int kSlots = 3;
-// y + gate bytes per chunk aimed at: small enough for ~8+ chunks at the
-// benchmark sizes (good overlap), large enough that a chunk's kernel is a
-// few microseconds against tens of microseconds of copies.
-constexpr int64_t kChunkTargetBytes = int64_t{8} << 20;
+// y + gate bytes per chunk aimed at.  Each copy carries a fixed cost, so
+// larger chunks pay less of it, while fewer chunks overlap less at the ends:
+// a sweep of 2-128 MB over the four prefill workloads measured 32 MB best or
+// within 1 % of best on each (8 MB: 9-16 % slower; some larger sizes dipped
+// on one workload or another).  Three slots measured as good as four or six.
+constexpr int64_t kChunkTargetBytes = int64_t{32} << 20;
 constexpr int64_t kAlign = 256;
 
 int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -69,7 +71,9 @@ cudaError_t pipe_init(HostPipe* hp) {
 }
 
 // Copy `n` rows of `width` elements between a strided host matrix and a
-// contiguous device block (one 1-D copy when the host rows are contiguous).
+// contiguous device block (one 1-D copy when the host rows are contiguous;
+// strided rows go as one 2-D copy, which measured as fast most of the time
+// but at half speed in some runs, hence the joint copy below).
 cudaError_t copy_rows(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch,
                       int64_t row_bytes, int64_t n, cudaMemcpyKind kind, cudaStream_t s) {
   if (dst_pitch == row_bytes && src_pitch == row_bytes)
@@ -112,6 +116,21 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
   while (chunk > 0 && kSlots * 3 * align_up(chunk * row_bytes) > workspace_bytes) --chunk;
   if (chunk < 1) return GGRN_ERR_ARG;
   const int64_t part = align_up(chunk * row_bytes);  // one tensor of one slot
+  // y and gate as two column ranges of one packed host matrix (a fused
+  // in-proj output) that cover at least 90 % of its rows: one contiguous
+  // copy per chunk, from the first used byte of its first row to the last
+  // used byte of its last row, into the slot's y and gate parts together;
+  // the kernel then reads the two ranges in place.
+  const char* yb = static_cast<const char*>(y_host);
+  const char* gb = static_cast<const char*>(gate_host);
+  const int64_t pitch = a.ys * es;
+  const char* lo = std::min(yb, gb);
+  const int64_t span = (std::max(yb, gb) - lo) + row_bytes;  // used bytes of a row
+  bool joint = rows > 1 && a.ys == a.gts && span <= pitch && 10 * 2 * row_bytes >= 9 * pitch;
+  if (joint) {
+    chunk = std::min(chunk, (2 * part - span) / pitch + 1);  // (n - 1) * pitch + span <= 2 * part
+    joint = chunk >= 1;
+  }
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -143,16 +162,29 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
     char* dout = dg + part;
     // host -> device, once the slot's previous output has left
     e = cudaStreamWaitEvent(hp->h2d, hp->freed[slot], 0);
-    if (e == cudaSuccess)
-      e = copy_rows(dy, row_bytes, yh + r0 * ysb, ysb, row_bytes, n, cudaMemcpyHostToDevice, hp->h2d);
-    if (e == cudaSuccess)
-      e = copy_rows(dg, row_bytes, gh + r0 * gsb, gsb, row_bytes, n, cudaMemcpyHostToDevice, hp->h2d);
+    const void *ky = dy, *kg = dg;  // the kernel's y and gate
+    int64_t kstride = width;
+    if (joint) {
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dy, lo + r0 * pitch, static_cast<size_t>((n - 1) * pitch + span),
+                            cudaMemcpyHostToDevice, hp->h2d);
+      ky = dy + (yb - lo);
+      kg = dy + (gb - lo);
+      kstride = a.ys;
+    } else {
+      if (e == cudaSuccess)
+        e = copy_rows(dy, row_bytes, yh + r0 * ysb, ysb, row_bytes, n, cudaMemcpyHostToDevice,
+                      hp->h2d);
+      if (e == cudaSuccess)
+        e = copy_rows(dg, row_bytes, gh + r0 * gsb, gsb, row_bytes, n, cudaMemcpyHostToDevice,
+                      hp->h2d);
+    }
     if (e == cudaSuccess) e = cudaEventRecord(hp->in[slot], hp->h2d);
-    // the kernel on the chunk (contiguous rows in the slot)
+    // the kernel on the chunk
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in[slot], 0);
     if (e == cudaSuccess) {
-      st = forward_call(call_args(dy, dg, w, dout, n, width, group_size, width, width, width, eps,
-                                  dtype, mode),
+      st = forward_call(call_args(ky, kg, w, dout, n, width, group_size, kstride, kstride, width,
+                                  eps, dtype, mode),
                         hp->comp);
       if (st == GGRN_OK) e = cudaEventRecord(hp->done[slot], hp->comp);
     }

@@ -179,7 +179,7 @@ int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w, 
                       int mode, void* workspace, int64_t workspace_bytes, void* cuda_stream);
 
 /* Device workspace in bytes for which ggrn_forward_host uses full-size
- * chunks (about 8 MB of y and gate per chunk, three slots); 0 for rows <= 0
+ * chunks (about 32 MB of y and gate per chunk, three slots); 0 for rows <= 0
  * or width <= 0. */
 int64_t ggrn_host_workspace_bytes(int64_t rows, int64_t width, int dtype);
 

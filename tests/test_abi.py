@@ -238,5 +238,5 @@ def test_host_pipeline_rejects_before_enqueueing():
     assert call(wsb=1000) == binding.ERR_ARG       # not one row per slot
     lib = g.load()
     need = lib.ggrn_host_workspace_bytes(4096, 7680, 2)
-    assert need == 3 * 3 * (-(-min(4096, (8 << 20) // (2 * 7680 * 2)) * 7680 * 2 // 256) * 256)
+    assert need == 3 * 3 * (-(-min(4096, (32 << 20) // (2 * 7680 * 2)) * 7680 * 2 // 256) * 256)
     assert lib.ggrn_host_workspace_bytes(0, 7680, 2) == 0

@@ -78,3 +78,20 @@ def test_ordered_on_the_callers_stream():
     torch.cuda.synchronize()
     assert torch.equal(back.cpu().view(torch.int16), out.view(torch.int16))
     assert not bool((out == -1280.0).any())
+
+
+@pytest.mark.parametrize("pw,ycol,gcol", [(9664, 64, 4864),    # joint copy, y not at row start
+                                          (9664, 4864, 0),     # joint copy, gate first
+                                          (14400, 0, 9600)])   # too much unused: 2-D copies
+def test_packed_host_buffers(pw, ycol, gcol):
+    rows, width, gs = 333, 4800, 100
+    gen = torch.Generator().manual_seed(pw + ycol)
+    packed = torch.randn(rows, pw, generator=gen).to(torch.bfloat16).pin_memory()
+    w = 1.0 + 0.1 * torch.randn(width, generator=gen)
+    y, gate = packed[:, ycol:ycol + width], packed[:, gcol:gcol + width]
+    ws = g.host_workspace(rows, width, torch.bfloat16, "cuda")
+    out = g.forward_host(y, gate, w.cuda(), group_size=gs, eps=1e-5, workspace=ws)
+    torch.cuda.synchronize()
+    host = ggrn_inputs.Inputs(y=y.contiguous(), gate=gate.contiguous(), w=w)
+    res = gpu_util.compare(out, host, gs, 1e-5, 0)
+    assert res["ok"], res
