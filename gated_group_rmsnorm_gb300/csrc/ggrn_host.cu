@@ -39,6 +39,25 @@ int64_t target_chunk_rows(int64_t rows, int64_t width, int es) {
   return std::min(rows, r);
 }
 
+// Row counts of the chunks, at most `t` each.  When there are enough rows,
+// the first two chunks are a quarter and a half of `t` and the last two
+// mirror them, so the copies of the two directions overlap sooner and longer
+// (+1-2 % end to end against equal chunks); the middle rows split evenly.
+int64_t chunk_rows_at(int64_t rows, int64_t t, int64_t c, int64_t* n_chunks) {
+  const int64_t q = std::max<int64_t>(1, t / 4), h = std::max<int64_t>(1, t / 2);
+  if (rows <= 2 * (q + h) + t) {  // equal chunks
+    *n_chunks = (rows + t - 1) / t;
+    return std::min(t, rows - c * t);
+  }
+  const int64_t mid = rows - 2 * (q + h);
+  const int64_t k = (mid + t - 1) / t;  // middle chunks
+  const int64_t m = (mid + k - 1) / k;
+  *n_chunks = k + 4;
+  if (c == 0 || c == k + 3) return q;
+  if (c == 1 || c == k + 2) return h;
+  return std::min(m, mid - (c - 2) * m);
+}
+
 // Streams and events of one device, created once (the first call there) and
 // shared by all calls on that device; `mu` keeps one call's enqueue
 // sequence whole when several host threads call at once.
@@ -154,8 +173,11 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
   char* oh = static_cast<char*>(out_host);
   char* ws = static_cast<char*>(workspace);
   const int64_t ysb = a.ys * es, gsb = a.gts * es, osb = a.os * es;
-  for (int64_t r0 = 0, c = 0; r0 < rows && e == cudaSuccess && st == GGRN_OK; r0 += chunk, ++c) {
-    const int64_t n = std::min(chunk, rows - r0);
+  int64_t n_chunks = 1;
+  chunk_rows_at(rows, chunk, 0, &n_chunks);
+  for (int64_t c = 0, r0 = 0, n = 0; c < n_chunks && e == cudaSuccess && st == GGRN_OK;
+       ++c, r0 += n) {
+    n = chunk_rows_at(rows, chunk, c, &n_chunks);
     const int slot = static_cast<int>(c % kSlots);
     char* dy = ws + slot * 3 * part;
     char* dg = dy + part;
