@@ -94,6 +94,7 @@ constexpr int kStreamWarps = 8;  // consumer warps per CTA (target)
 constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
 // Ring stages (at most; the shared-memory budget may allow fewer).
 constexpr int64_t kStreamMaxStages = 2;
+constexpr int64_t kStreamMinUnitsPerSlot = 12;
 constexpr int64_t kStreamMaxWeightBytes = 64 * 1024;
 
 int elem_size(int dtype) { return dtype == kF32 ? 4 : 2; }
@@ -366,7 +367,7 @@ bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t max_stages, int* cps, 
 // Q = 2 when they are an odd multiple of 8 (a pair of groups is then whole
 // 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
 // vectors, every unit is a 16-byte multiple, and (unless forced) there are
-// at least two units per CTA slot.
+// at least kStreamMinUnitsPerSlot units per CTA slot.
 int plan_stream(const Args& a, Plan* p, bool forced) {
   const int es = elem_size(a.dtype);
   const int64_t gbytes = a.gs * es;
@@ -456,7 +457,11 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   if (!stream_smem(stage_bytes, wb, max_stages, &cps, &ns, &wstage))
     return GGRN_ERR_UNSUPPORTED;
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
-  if (!forced && units < 2 * gmax) return GGRN_ERR_UNSUPPORTED;
+  // Automatic selection streams only with 12+ units per CTA slot: below that
+  // the ring's fill and drain cost more than the register-resident TEAM
+  // kernel loses (measured crossovers: about 13 units per slot on the
+  // 960-wide prefill groups, 18 on 128-wide heads, 11 on the odd span).
+  if (!forced && units < kStreamMinUnitsPerSlot * gmax) return GGRN_ERR_UNSUPPORTED;
   // static schedule: equal units per CTA, so the last wave ends together
   const int64_t per_cta = ceil_div(units, gmax);
   p->path = kStream;

@@ -33,11 +33,13 @@ def _case(name, rows, seed=0):
 
 def _fwd(wl, dev, out=None):
     return g.forward(dev.y, dev.gate, dev.w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode,
-                     out=out)
+                     out=out, path=g.PATH_STREAM)
 
 
-@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 1500), ("gdn_onnx", 2600),
-                                       ("strided_odd_span", 1900)])
+# rows at which automatic selection streams (12+ units per CTA slot), so that
+# the library's own graph API, which selects automatically, records STREAM too
+@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 4096), ("gdn_onnx", 5600),
+                                       ("strided_odd_span", 9200)])
 def test_claimed_schedule_matches_oracle_and_graph_replay(name, rows):
     g.fault_status(clear=True)
     wl, host, dev = _case(name, rows)
