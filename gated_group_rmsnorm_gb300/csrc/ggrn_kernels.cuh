@@ -512,9 +512,16 @@ __global__ void __launch_bounds__(256, team_min_blocks(MODE)) k_team(const KPara
 // (double-buffered by loop parity, so one barrier per group suffices) and
 // every thread adds them in the same order.
 // ---------------------------------------------------------------------------
+// Resident CTAs per SM the register budget targets (CTAs of at most 256
+// threads): MAMBA2 six (40 registers; a 28-byte spill is cheaper than the
+// latency fewer CTAs leave exposed: 6.49 -> 6.80 TB/s on 5120-wide groups,
+// where seven or eight spill heavily and fall to 4 TB/s); ONNX four.
+constexpr int wide_min_blocks(int mode, int maxt) {
+  return maxt <= 256 ? (mode == kOnnx ? 4 : 6) : 1;
+}
+
 template <typename T, int MODE, int VPL, int MAXT>
-__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? (MODE == kOnnx ? 4 : 5) : 1)
-    k_wide(const KParams p) {
+__global__ void __launch_bounds__(MAXT, wide_min_blocks(MODE, MAXT)) k_wide(const KParams p) {
   constexpr int E = Elem<T>::E;
   __shared__ float red[2][32];
   pdl_wait();
