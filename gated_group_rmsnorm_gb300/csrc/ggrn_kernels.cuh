@@ -871,8 +871,14 @@ cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
       }
       break;
     case kWide:
-      if (p.vpl == 4 && p.block <= 256) return launch_kernel(k_wide<T, MODE, 4, 256>, k, p, s);
-      if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 1024>, k, p, s);
+      if (p.block <= 256) {
+        if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 256>, k, p, s);
+        if (p.vpl == 1) return launch_kernel(k_wide<T, MODE, 1, 256>, k, p, s);
+      } else {
+        if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 1024>, k, p, s);
+        if (p.vpl == 2) return launch_kernel(k_wide<T, MODE, 2, 1024>, k, p, s);
+        if (p.vpl == 1) return launch_kernel(k_wide<T, MODE, 1, 1024>, k, p, s);
+      }
       break;
     case kStraddle:
       return launch_straddle<T, MODE>(k, p, s);

@@ -149,16 +149,22 @@ def test_plan_selects_families():
     assert _plan(4096, 48 * 12, 12, 2).path != g.PATH_STREAM
     # a width that is not a multiple of the vector goes to the scalar path
     assert _plan(4, 300, 100, 2).path == g.PATH_SCALAR
-    # decode (one row, 8 groups): one warp per CTA spreads the groups over SMs
+    # decode (one row, 8 groups): a CTA of 128 threads per group, one 16-byte
+    # vector per thread
     p = _plan(1, 7680, 960, 2)
-    assert (p.path, p.block_threads, p.grid_blocks) == (g.PATH_TEAM, 32, 8)
+    assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 128, 1, 8)
+    # still few groups (16 rows x 8 = 128 <= 152 SMs); then TEAM
+    assert _plan(16, 7680, 960, 2).path == g.PATH_WIDE
+    assert _plan(64, 7680, 960, 2).path == g.PATH_TEAM
     # tiny groups and misaligned views fall back to element loads
     assert _plan(8, 12, 3, 2).path == g.PATH_SCALAR
     assert _plan(8, 960, 960, 2, off=1).path == g.PATH_SCALAR
     assert _plan(8, 960, 960, 2, ys=961).path == g.PATH_SCALAR
-    # f32: 4 elements per vector
-    p = _plan(8, 128, 128, 0)
+    # f32: 4 elements per vector; with few groups one vector per thread
+    p = _plan(256, 128, 128, 0)
     assert (p.path, p.elems_per_vec, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 8, 4)
+    p = _plan(8, 128, 128, 0)
+    assert (p.path, p.elems_per_vec, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 4, 32, 1)
     # a group too wide for registers goes to the scalar two-pass path
     assert _plan(2, 1 << 16, 1 << 16, 2).path == g.PATH_SCALAR
     # rows == 0 still plans, with nothing to launch
