@@ -873,6 +873,7 @@ cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
     case kWide:
       if (p.block <= 256) {
         if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 256>, k, p, s);
+        if (p.vpl == 2) return launch_kernel(k_wide<T, MODE, 2, 256>, k, p, s);
         if (p.vpl == 1) return launch_kernel(k_wide<T, MODE, 1, 256>, k, p, s);
       } else {
         if (p.vpl == 4) return launch_kernel(k_wide<T, MODE, 4, 1024>, k, p, s);

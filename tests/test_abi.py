@@ -129,6 +129,13 @@ def test_plan_selects_families():
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
     p = _plan(16384, 5120, 5120, 2)
     assert (p.path, p.block_threads, p.vec_per_lane, p.grid_blocks) == (g.PATH_WIDE, 160, 4, 16384)
+    # fewer rows of it: more threads per group (1 or 2 vectors each)
+    p = _plan(256, 5120, 5120, 2)
+    assert (p.path, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 640, 1)
+    p = _plan(512, 5120, 5120, 2)
+    assert (p.path, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 320, 2)
+    p = _plan(500, 2048, 2048, 2)
+    assert (p.path, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 128, 2)
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
     # 9664: streamed in pairs of groups (25 whole 16-byte vectors) by teams of
     # 4 lanes x 7 vectors; units of 5 whole rows (15 consumer warps x 8 teams
