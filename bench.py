@@ -193,6 +193,19 @@ def recorded_traffic(workload: str) -> tuple[float | None, str]:
     return float(found["dram_bytes_per_launch"]), found.get("note", "ncu capture")
 
 
+def recorded_ncu_gbs(workload: str) -> float | None:
+    """(DRAM read + write bytes) / duration of the recorded ncu capture of the
+    workload's kernel (one cold launch), if taken on the current sources."""
+    if recorded_traffic(workload)[0] is None:
+        return None
+    with open(TRAFFIC_FILE) as fh:
+        for line in fh:
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if kv.get("workload") == workload and "ncu_gbs" in kv:
+                return float(kv["ncu_gbs"])
+    return None
+
+
 # ---------------------------------------------------------------------------
 # Our arm.
 # ---------------------------------------------------------------------------
@@ -467,7 +480,11 @@ def run_ours(args) -> None:
                      "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
                      "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": bytes_per_step,
-                     "traffic_note": traffic_note},
+                     "traffic_note": traffic_note,
+                     "ncu_dram_gbs": recorded_ncu_gbs(wl.name),
+                     "ncu_dram_gbs_note": "DRAM read+write bytes over the duration of one cold "
+                                          "launch under ncu; writes still dirty in L2 at the "
+                                          "kernel's end are not counted"},
         "clocks": clocks,
         "gpu_launches": args.steps,
         "e2e": e2e,
