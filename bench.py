@@ -314,7 +314,7 @@ def _e2e(g, wl, steps: int, device) -> dict:
     def step():
         g.forward_host(y_h, g_h, w_d, group_size=wl.group_size, eps=wl.eps, mode=wl.mode,
                        out=out_h, workspace=ws)
-    for _ in range(3):
+    for _ in range(5):
         step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -635,7 +635,7 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", choices=sorted(ggrn_inputs.WORKLOADS), default="mamba2_prefill")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-e2e", action="store_true")
