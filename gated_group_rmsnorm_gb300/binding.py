@@ -31,7 +31,8 @@ MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
            "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc",
-           "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_host_workspace_bytes")
+           "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_host_workspace_bytes",
+           "ggrn_selftest_wait_timeout")
 
 
 class GgrnError(RuntimeError):
@@ -86,6 +87,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
         L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
         L.ggrn_forward.restype = ci
+        L.ggrn_selftest_wait_timeout.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, vp]
+        L.ggrn_selftest_wait_timeout.restype = ci
         L.ggrn_forward_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci,
                                         vp, i64, vp]
         L.ggrn_forward_host.restype = ci

@@ -682,6 +682,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.rows_per_unit = p.rows_per_unit;
   k.rows = a.rows;
   k.fault = nullptr;
+  k.no_copies = 0;
   k.sched = nullptr;
   k.epoch = 0;
   k.eps = a.eps;
@@ -938,6 +939,35 @@ extern "C" int ggrn_forward_noalloc(const void* y, const void* gate, const void*
       case kF16: e = launch_f16(k, p, a.mode, s); break;
       default: e = launch_bf16(k, p, a.mode, s); break;
     }
+  }
+  if (e != cudaSuccess) {
+    tl_last_cuda_error = e;
+    return GGRN_ERR_CUDA;
+  }
+  return GGRN_OK;
+}
+
+extern "C" int ggrn_selftest_wait_timeout(const void* y, const void* gate, const void* w,
+                                          void* out, int64_t rows, int64_t width,
+                                          int64_t group_size, int dtype, void* cuda_stream) {
+  const Args a = make_args(y, gate, w, out, rows, width, group_size, width, width, width, 1e-5f,
+                           dtype, kMamba2);
+  int st = validate(a);
+  if (st != GGRN_OK) return st;
+  if (rows == 0) return GGRN_ERR_SHAPE;
+  if (!vector_layout_ok(a)) return GGRN_ERR_ALIGN;
+  Plan p;
+  if ((st = plan_stream(a, &p, /*forced=*/true)) != GGRN_OK) return st;
+  KParams k = make_params(a, p);
+  k.fault = fault_word();
+  if (!k.fault) return GGRN_ERR_CUDA;
+  k.no_copies = 1;
+  const cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e;
+  switch (a.dtype) {
+    case kF32: e = launch_f32(k, p, a.mode, s); break;
+    case kF16: e = launch_f16(k, p, a.mode, s); break;
+    default: e = launch_bf16(k, p, a.mode, s); break;
   }
   if (e != cudaSuccess) {
     tl_last_cuda_error = e;

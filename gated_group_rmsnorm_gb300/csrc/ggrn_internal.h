@@ -102,6 +102,7 @@ struct KParams {
   int unit_mode;
   int rows_per_unit;
   int64_t rows;
+  int no_copies;              // STREAM self-test: the producer issues nothing
   unsigned long long* sched;  // STREAM: unit-claim word, or NULL (static schedule)
   uint32_t epoch;             // STREAM: this launch's claim epoch (nonzero)
   float eps;

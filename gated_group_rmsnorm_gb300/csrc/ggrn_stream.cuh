@@ -245,6 +245,9 @@ template <typename T>
 __device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx& c) {
   constexpr int ES = sizeof(T);
   const int64_t gs = p.gs;
+  // self-test of the failure path: no copy, no arrival; every consumer wait
+  // runs out, records its fault bit and returns
+  if (p.no_copies) return;
   if (c.wbytes) {
     mbar_expect_tx(c.wbar, c.wbytes);
     bulk_g2s(smem_u32(c.wsm), p.w, c.wbytes, c.wbar);

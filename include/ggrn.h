@@ -264,6 +264,19 @@ int ggrn_fault_status(uint32_t* flags, int clear);
 const char* ggrn_last_cuda_error(void);
 
 /*
+ * ggrn_selftest_wait_timeout -- exercise the STREAM family's failure path.
+ * Launches the streaming kernel (MAMBA2, contiguous rows) on the given
+ * buffers with its producer issuing nothing: each consumer's bounded wait
+ * runs out (about a second), sets bit 1 of the status word and ends; no
+ * buffer is read or written and the CUDA context stays usable.  Arguments as
+ * in ggrn_forward (row strides = width, eps fixed); the buffers only have to
+ * be valid for the shape.  Read the result with ggrn_fault_status.
+ */
+int ggrn_selftest_wait_timeout(const void* y, const void* gate, const void* w, void* out,
+                               int64_t rows, int64_t width, int64_t group_size, int dtype,
+                               void* cuda_stream);
+
+/*
  * ggrn_forward_noalloc -- an addition of this library; the pages have no
  * counterpart.
  *
