@@ -317,19 +317,27 @@ def _e2e(g, wl, steps: int, device) -> dict:
     for _ in range(5):
         step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    # three timed windows of `steps` steps; the median is reported (the host
+    # link shows occasional transients of a few tens of ms from outside this
+    # process), all three are listed
+    windows = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        windows.append(e0.elapsed_time(e1))
+    ms = sorted(windows)[1]
     es = out_h.element_size()
-    h2d_bytes = 2 * wl.rows * width * es   # the y and gate columns (strided rows copied in 2-D)
+    h2d_bytes = 2 * wl.rows * width * es   # the y and gate columns of every row
     d2h_bytes = wl.rows * width * es
     return {"value": round(wl.algorithmic_bytes() * steps / (ms / 1e3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
             "ms_per_step": round(ms / steps, 4),
+            "windows_gbs": [round(wl.algorithmic_bytes() * steps / (t / 1e3) / 1e9, 2)
+                            for t in windows],
             "api": "forward_host (ggrn_forward_host: chunks cycle through a device workspace, "
                    "host-to-device copies, kernels and device-to-host copies overlapped)"}
 
