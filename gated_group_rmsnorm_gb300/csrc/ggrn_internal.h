@@ -57,6 +57,8 @@ struct Plan {
   int64_t total_groups = 0;
   int unit_mode = 0;           // 0 flat (contiguous rows), 1 chunk of a row, 2 whole rows
   int rows_per_unit = 0;       // unit_mode 2
+  int64_t head_units = 0;      // unit_mode 0 and 2: short units first (see KParams)
+  int head_size = 0;
   uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
   int ctas_per_sm = 0;
 };
@@ -101,6 +103,11 @@ struct KParams {
   int ug;
   int unit_mode;
   int rows_per_unit;
+  // STREAM flat and row units: head_units units of head_size first, then
+  // units of the normal size (sizes in groups for flat units, rows for row
+  // units)
+  int64_t head_units;
+  int head_size;
   int64_t rows;
   int no_copies;              // STREAM self-test: the producer issues nothing
   unsigned long long* sched;  // STREAM: unit-claim word, or NULL (static schedule)

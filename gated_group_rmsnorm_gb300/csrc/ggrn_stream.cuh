@@ -237,6 +237,18 @@ __device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned cha
   return c;
 }
 
+// Flat and row units cut a sequence of n groups or rows: head_units units of
+// head_size, then units of `mid`, the last one clipped at n.  Returns unit
+// u's first element and sets its length.
+__device__ __forceinline__ int64_t unit_span(const KParams& p, int64_t u, int64_t mid, int64_t n,
+                                             int64_t* len) {
+  const bool head = u < p.head_units;
+  const int64_t first =
+      head ? u * p.head_size : p.head_units * p.head_size + (u - p.head_units) * mid;
+  *len = min(head ? static_cast<int64_t>(p.head_size) : mid, n - first);
+  return first;
+}
+
 // The producer lane: stage the weight, then stream this CTA's units into the
 // ring, each stage's unit recorded in unit_of; after the last unit a stage
 // with unit -1 (completed by a plain arrive) tells the consumers to stop.
@@ -280,8 +292,8 @@ __device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx
     unsigned char* st = c.ring + static_cast<size_t>(2) * s * c.sb;
     if (p.unit_mode == kUnitRows) {
       // R whole rows, one copy per row and tensor, packed in the slot
-      const int64_t row0 = u * p.rows_per_unit;
-      const int64_t nr = min(static_cast<int64_t>(p.rows_per_unit), p.rows - row0);
+      int64_t nr;
+      const int64_t row0 = unit_span(p, u, p.rows_per_unit, p.rows, &nr);
       const uint32_t rb = static_cast<uint32_t>(p.width * ES);
       mbar_expect_tx(full, static_cast<uint32_t>(2 * nr) * rb);
       for (int64_t r = 0; r < nr; ++r) {
@@ -292,8 +304,7 @@ __device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx
     } else {
       int64_t yo, go, ngroups;
       if (p.unit_mode == kUnitFlat) {
-        const int64_t g0 = u * p.ug;
-        ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - g0);
+        const int64_t g0 = unit_span(p, u, p.ug, p.total_groups, &ngroups);
         yo = go = g0 * gs;
       } else {
         const int64_t row = div_by(u, p.units_per_row, p.div_magic);
@@ -334,15 +345,15 @@ struct UnitPos {
 __device__ __forceinline__ UnitPos unit_pos(const KParams& p, int64_t u) {
   UnitPos r{0, 0, 0, 0};
   if (p.unit_mode == kUnitFlat) {
-    r.g0 = u * p.ug;
-    r.ngroups = min(static_cast<int64_t>(p.ug), p.total_groups - r.g0);
+    r.g0 = unit_span(p, u, p.ug, p.total_groups, &r.ngroups);
   } else if (p.unit_mode == kUnitChunk) {
     r.row = div_by(u, p.units_per_row, p.div_magic);
     r.col = (u - r.row * p.units_per_row) * p.ug * p.gs;
     r.ngroups = p.ug;
   } else {
-    r.row = u * p.rows_per_unit;
-    r.ngroups = min(static_cast<int64_t>(p.rows_per_unit), p.rows - r.row) * p.groups;
+    int64_t nr;
+    r.row = unit_span(p, u, p.rows_per_unit, p.rows, &nr);
+    r.ngroups = nr * p.groups;
   }
   return r;
 }

@@ -109,21 +109,23 @@ def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
 
 def test_plan_selects_families():
     # Mamba-2 prefill 4096x7680, group 960: streamed, two rows (16 groups) per
-    # unit, one warp per group (32 lanes x 4 vectors of 16 bytes), 16 consumer
-    # warps + 1 producer warp, one CTA on each of 152 SMs claiming units
+    # unit after a first unit of one row for each of the 152 CTA slots, one
+    # warp per group (32 lanes x 4 vectors of 16 bytes), 16 consumer warps +
+    # 1 producer warp, one CTA on each of 152 SMs claiming units
     p = _plan(4096, 7680, 960, 2)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads) == \
-        (g.PATH_STREAM, 32, 4, 2048, 17 * 32)
+        (g.PATH_STREAM, 32, 4, 152 + (4096 - 152) // 2, 17 * 32)
     assert p.grid_blocks == 152
     # the same shape on the register-resident family: one warp per group
     p = _plan(4096, 7680, 960, 2, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
     # gated-DeltaNet per-head, C=128 fp16 (16 vectors): 4-lane teams with 4
     # vectors each, 8 groups per warp; 6 consumer warps, units of 48 groups
-    # of the contiguous rows (the last one partial), 2 CTAs per SM
+    # of the contiguous rows (the last one partial) after a first unit of 24
+    # for each of the 304 CTA slots, 2 CTAs per SM
     p = _plan(32768, 4096, 128, 1, mode=1)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
-        (g.PATH_STREAM, 4, 4, -(-32768 * 32 // 48), 7 * 32, 304)
+        (g.PATH_STREAM, 4, 4, 304 + -(-(32768 * 32 - 304 * 24) // 48), 7 * 32, 304)
     p = _plan(32768, 4096, 128, 1, mode=1, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 4)
     # wide single group of 5120 (640 vectors): one 160-thread CTA per group
@@ -139,10 +141,11 @@ def test_plan_selects_families():
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
     # 9664: streamed in pairs of groups (25 whole 16-byte vectors) by teams of
     # 4 lanes x 7 vectors; units of 5 whole rows (15 consumer warps x 8 teams
-    # x 2 groups = 240 groups), one CTA per SM
+    # x 2 groups = 240 groups) after a first unit of 4 rows for each CTA
+    # slot, one CTA per SM
     p = _plan(65536, 4800, 100, 2, ys=9664)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
-        (g.PATH_STREAM, 4, 7, -(-65536 // 5), 16 * 32, 152)
+        (g.PATH_STREAM, 4, 7, 152 + -(-(65536 - 152 * 4) // 5), 16 * 32, 152)
     # register-resident teams of 8 lanes x 4 vectors, 24 pairs per row
     p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 8, 4, 24 * 65536)
@@ -253,3 +256,17 @@ def test_host_pipeline_rejects_before_enqueueing():
     need = lib.ggrn_host_workspace_bytes(4096, 7680, 2)
     assert need == 3 * 3 * (-(-min(4096, (32 << 20) // (2 * 7680 * 2)) * 7680 * 2 // 256) * 256)
     assert lib.ggrn_host_workspace_bytes(0, 7680, 2) == 0
+
+
+def test_stream_short_first_units():
+    """A short first unit per CTA slot once the rest fills a full unit per
+    slot: units = slots + ceil((n - slots * head) / unit)."""
+    # prefill (flat, 152 slots, head 8 of 16 groups, 8 groups a row)
+    for rows, units in ((455, -(-455 * 8 // 16)), (456, 152 + 152), (457, 152 + -(-(457 * 8 - 1216) // 16))):
+        assert _plan(rows, 7680, 960, 2, path=g.PATH_STREAM).items == units, rows
+    # odd span (rows of 48 groups, 152 slots, head 4 of 5 rows)
+    for rows, units in ((1367, -(-1367 // 5)), (1368, 152 + 152), (1369, 152 + 153)):
+        assert _plan(rows, 4800, 100, 2, ys=9664, path=g.PATH_STREAM).items == units, rows
+    # chunk units (part of a row each) keep one size
+    p = _plan(4096, 3 * 4096, 4096 // 4, 2, ys=4 * 4096, path=g.PATH_STREAM)
+    assert p.items % 4096 == 0

@@ -115,3 +115,42 @@ def test_many_launches_cycle_the_claim_words():
     for o in outs:
         assert torch.equal(_bits(o), _bits(ref))
     assert g.fault_status() == 0
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+# Row counts around the point where each CTA slot's first unit becomes a
+# short one (a half unit of groups for flat units, one row fewer for row
+# units): it applies once the rest still fills a full unit per slot.
+#   mamba2_prefill, flat, 1 CTA/SM: 8 of 16 groups first -> from 3 x SMs rows
+#   gdn_onnx, flat, 2 CTAs/SM: 24 of 48 groups first -> from 4.5 x SMs rows
+#   strided_odd_span, rows, 1 CTA/SM: 4 of 5 rows first -> from 9 x SMs rows
+@pytest.mark.parametrize("name,per_sm", [("mamba2_prefill", 3.0), ("gdn_onnx", 4.5),
+                                         ("strided_odd_span", 9.0)])
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_short_first_units_threshold(name, per_sm, delta):
+    g.fault_status(clear=True)
+    rows = int(per_sm * _sms()) + delta
+    wl, host, dev = _case(name, rows, seed=rows)
+    pl = g.plan(dev.y, dev.gate, dev.w, group_size=wl.group_size, mode=wl.mode, path=g.PATH_STREAM)
+    assert pl["path"] == g.PATH_STREAM
+    eager = _fwd(wl, dev)
+    torch.cuda.synchronize()
+    res = gpu_util.compare(eager, host, wl.group_size, wl.eps, wl.mode)
+    assert res["ok"], res
+    out = torch.empty_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _fwd(wl, dev, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _fwd(wl, dev, out=out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(out), _bits(eager))
+    assert g.fault_status() == 0
