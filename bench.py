@@ -30,6 +30,7 @@ import ctypes
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -295,6 +296,61 @@ def _cpu_baseline(wl, budget_s: float = 10.0) -> dict:
                       f"single-threaded C++ oracle"}
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def _cpu_baseline_all_cores(wl, budget_s: float = 5.0) -> dict:
+    """The same per-row oracle code on every host core: one thread per core,
+    each running the single-threaded oracle over its own block of sample rows
+    until the budget is spent (the oracle's C call releases the GIL)."""
+    import concurrent.futures
+    import oracle
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    per = max(1, min(64, wl.rows // threads))
+    swl = wl.with_rows(per * threads)
+    inp = ggrn_inputs.make_inputs(swl)
+    out = torch.empty((swl.rows, wl.width), dtype=wl.dtype)
+    orc = oracle.default()
+    deadline = time.perf_counter() + budget_s
+
+    def work(t):
+        sl = slice(t * per, (t + 1) * per)
+        reps = 0
+        while True:
+            orc.forward(inp.y[sl], inp.gate[sl], inp.w, group_size=wl.group_size, eps=wl.eps,
+                        mode=wl.mode, out=out[sl])
+            reps += 1
+            if time.perf_counter() >= deadline:
+                return reps
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        reps = list(ex.map(work, range(threads)))
+    el = time.perf_counter() - t0
+    bytes_ = wl.with_rows(per).algorithmic_bytes() * sum(reps)
+    return {"value": round(bytes_ / el / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "rows_per_s": round(per * sum(reps) / el, 1),
+            "cpu_model": _cpu_model(), "hardware_threads": os.cpu_count(),
+            "sample": f"{threads} threads x {per} rows of {wl.name} (same recipe), "
+                      f"{sum(reps)} passes in all, {el:.1f} s, the single-threaded C++ oracle "
+                      f"per thread"}
+
+
 def _e2e(g, wl, steps: int, device) -> dict:
     """Public API with pinned host buffers: every step is one forward_host
     call (host y and gate in, host out back; the library overlaps the
@@ -455,6 +511,7 @@ def run_ours(args) -> None:
     extra = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         extra["cpu_baseline"] = _cpu_baseline(wl, args.cpu_seconds)
+        extra["cpu_baseline_all_cores"] = _cpu_baseline_all_cores(wl, args.cpu_seconds / 2)
     e2e = None
     if not args.no_e2e:
         e2e = _e2e(g, wl, args.e2e_steps, device)
