@@ -373,13 +373,6 @@ bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t max_stages, int* cps, 
   return *ns >= 2;
 }
 
-// STREAM: persistent CTAs fed by bulk copies of row chunks ("units" of ug
-// whole groups).  A team takes an item of Q groups: Q = 1 when a group's
-// bytes are a multiple of 16 (or of 8, with 8-byte shared-memory vectors),
-// Q = 2 when they are an odd multiple of 8 (a pair of groups is then whole
-// 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
-// vectors, every unit is a 16-byte multiple, and (unless forced) there are
-// at least kStreamMinUnitsPerSlot units per CTA slot.
 // Size of the short first unit of each CTA slot of a streaming launch
 // (groups for flat units, rows for row units; 0: none).  A first stage of
 // fewer bytes lands sooner, so compute starts sooner while the ring fills.
@@ -392,6 +385,13 @@ int64_t stream_head_size(int mode, int64_t mid, int Q) {
   return hs > 0 && hs < mid ? hs : 0;
 }
 
+// STREAM: persistent CTAs fed by bulk copies of row chunks ("units" of ug
+// whole groups).  A team takes an item of Q groups: Q = 1 when a group's
+// bytes are a multiple of 16 (or of 8, with 8-byte shared-memory vectors),
+// Q = 2 when they are an odd multiple of 8 (a pair of groups is then whole
+// 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
+// vectors, every unit is a 16-byte multiple, and (unless forced) there are
+// at least kStreamMinUnitsPerSlot units per CTA slot.
 int plan_stream(const Args& a, Plan* p, bool forced) {
   const int es = elem_size(a.dtype);
   const int64_t gbytes = a.gs * es;
@@ -513,9 +513,25 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->w_smem_bytes = static_cast<uint32_t>(wstage);
   // ring, weight, barriers full/empty/weight, unit of each stage
   p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes +
-                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 1) + 8 * ns);
+                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 2) + 8 * ns);
   p->div_magic = mode == 1 ? div_magic(units, upr) : 0;
   p->div_magic2 = div_magic(total, gpr);
+  // Teams of 4 lanes, 8 to a warp: an 8-lane phase of a shared-memory load
+  // holds two teams, each reading 4 consecutive 16-byte slots of its item.
+  // Consecutive items start d slots apart (mod the 8 slots of a 128-byte
+  // bank row); two teams on items d apart overlap unless d = 4.  So the
+  // teams sharing a phase take items 4 apart (d odd) or 2 apart (d = 2, 6):
+  // the odd span (pairs of 200 bf16, d = 1) went from 8.1 to about 4
+  // wavefronts per load and 6450 -> 6546 GB/s.  For d = 0 (the 128-wide
+  // fp16 heads) only walking the second team's vectors from its second one
+  // would help; that removed the conflicts but cost 5.8 % more instructions
+  // and measured 2 % slower, so those teams stay in order.
+  p->team_map = kTeamsInOrder;
+  if (lanes == 4 && sv == 16) {
+    const int64_t d = (gbytes * Q / 16) % 8;
+    if (d % 2 == 1) p->team_map = kTeamsApart4;
+    else if (d == 2 || d == 6) p->team_map = kTeamsApart2;
+  }
   // a short first unit for each CTA slot (flat units keep starting on
   // 16-byte boundaries and holding whole items)
   const int64_t mid = mode == 0 ? ug : rpu;
@@ -708,6 +724,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.rows_per_unit = p.rows_per_unit;
   k.head_units = p.head_units;
   k.head_size = p.head_size;
+  k.team_map = p.team_map;
   k.rows = a.rows;
   k.fault = nullptr;
   k.no_copies = 0;

@@ -10,6 +10,9 @@ namespace ggrn {
 enum Mode : int { kMamba2 = 0, kOnnx = 1 };
 enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 enum Path : int { kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4, kStream = 5 };
+// STREAM with 8 teams per warp: how the teams of a warp's pass take its 8
+// consecutive items (see plan_stream)
+enum TeamMap : int { kTeamsInOrder = 0, kTeamsApart2 = 1, kTeamsApart4 = 2 };
 
 // Validated arguments of one call.
 struct Args {
@@ -59,6 +62,7 @@ struct Plan {
   int rows_per_unit = 0;       // unit_mode 2
   int64_t head_units = 0;      // unit_mode 0 and 2: short units first (see KParams)
   int head_size = 0;
+  int team_map = kTeamsInOrder;
   uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
   int ctas_per_sm = 0;
 };
@@ -108,6 +112,7 @@ struct KParams {
   // units)
   int64_t head_units;
   int head_size;
+  int team_map;            // STREAM: TeamMap
   int64_t rows;
   int no_copies;              // STREAM self-test: the producer issues nothing
   unsigned long long* sched;  // STREAM: unit-claim word, or NULL (static schedule)

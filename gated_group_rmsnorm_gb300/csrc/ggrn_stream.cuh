@@ -195,7 +195,7 @@ __device__ __forceinline__ int64_t claim_resolve(unsigned long long* w, uint32_t
 // ---------------------------------------------------------------------------
 // Pieces of the streaming kernel.  Dynamic shared memory:
 // [stages][y slot | gate slot], the weight area, then the barriers
-// full[NS], empty[NS], wbar, and the unit of each stage (int64 [NS]).
+// full[NS], empty[NS], wbar, sbar, and the unit of each stage (int64 [NS]).
 // ---------------------------------------------------------------------------
 struct StreamCtx {
   unsigned char* ring;
@@ -204,6 +204,7 @@ struct StreamCtx {
   uint32_t sb;           // bytes of one tensor's slot (128-aligned)
   uint32_t wbytes;       // 0: the weight is read from global memory
   uint32_t full0, empty0, wbar;
+  uint32_t sbar;         // every consumer thread done permuting the staged weight
   int NS, W;
 };
 
@@ -222,13 +223,15 @@ __device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned cha
   c.full0 = smem_u32(bars);
   c.empty0 = smem_u32(bars + c.NS);
   c.wbar = smem_u32(bars + 2 * c.NS);
-  c.unit_of = reinterpret_cast<long long*>(bars + 2 * c.NS + 1);
+  c.sbar = smem_u32(bars + 2 * c.NS + 1);
+  c.unit_of = reinterpret_cast<long long*>(bars + 2 * c.NS + 2);
   if (threadIdx.x == 0) {
     for (int s = 0; s < c.NS; ++s) {
       mbar_init(c.full0 + 8 * s, 1);
       mbar_init(c.empty0 + 8 * s, c.W);
     }
     mbar_init(c.wbar, 1);
+    mbar_init(c.sbar, 32 * c.W);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -377,10 +380,39 @@ __device__ __forceinline__ void group_place(const KParams& p, const UnitPos& up,
   }
 }
 
-// f32 weight of SE columns at wi (shared memory when staged).
-template <int SE>
+// The staged f32 weight of MAMBA2 with 16-bit T is read 32 bytes (one
+// vector's 8 columns) per lane, lanes 32 bytes apart: as stored, two lanes
+// of every 8 would meet on the same banks.  So the staged copy is permuted
+// once per CTA: in each 32-byte block whose index has bit 2 set the two
+// 16-byte halves trade places, and 8 consecutive blocks then read either
+// half from 8 distinct 16-byte bank groups (prefill 960-wide groups: 6078
+// -> 6171 GB/s in alternating runs).
+__device__ __forceinline__ void swap_weight_halves(unsigned char* wsm, uint32_t wbytes, int tid,
+                                                   int nthreads) {
+  for (uint32_t b = 4u + 8u * (tid >> 2) + (tid & 3); b < wbytes / 32u; b += 2u * nthreads) {
+    uint4* h = reinterpret_cast<uint4*>(wsm + 32u * b);
+    const uint4 lo = h[0], hi = h[1];
+    h[0] = hi;
+    h[1] = lo;
+  }
+}
+
+// f32 weight of SE columns at wi (shared memory when staged; SWZ: the
+// staged copy has its halves permuted as above).
+template <int SE, bool SWZ>
 __device__ __forceinline__ void load_w_cols(const KParams& p, const StreamCtx& c, int64_t wi,
                                             float (&wv)[SE]) {
+  if constexpr (SWZ && SE == 8) {
+    if (c.wbytes) {
+      const unsigned char* blk = c.wsm + 4 * wi;
+      const uint32_t x = 16u * ((static_cast<uint32_t>(wi) >> 5) & 1u);  // bit 2 of wi / 8
+      const float4 lo = *reinterpret_cast<const float4*>(blk + x);
+      const float4 hi = *reinterpret_cast<const float4*>(blk + (16u - x));
+      wv[0] = lo.x, wv[1] = lo.y, wv[2] = lo.z, wv[3] = lo.w;
+      wv[4] = hi.x, wv[5] = hi.y, wv[6] = hi.z, wv[7] = hi.w;
+      return;
+    }
+  }
 #pragma unroll
   for (int q = 0; q < SE; q += 4 > SE ? SE : 4) {
     if (SE >= 4) {
@@ -430,6 +462,20 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
     return;
   }
+  // (for teams of 8+ lanes, whose 8-lane phases read consecutive blocks;
+  // narrower teams read the weight at scattered columns: on the paired
+  // 4-lane teams of the odd span the permutation measured 0.35 % slower)
+  constexpr bool kSwz = MODE == kMamba2 && SE == 8 && Q == 1 && L >= 8;
+  if (kSwz && wbytes) {
+    // permute the staged weight (all consumer threads), then wait until
+    // every consumer thread has finished its share (bounded like every wait)
+    swap_weight_halves(wsm, wbytes, threadIdx.x, 32 * W);
+    mbar_arrive(c.sbar);
+    if (!mbar_wait(c.sbar, 0)) {
+      if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
+      return;
+    }
+  }
 
   // ---------------- consumers ----------------
   // A team takes an "item" of Q consecutive groups.  Q = 2 pairs groups whose
@@ -438,6 +484,16 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
   // middle, its low half ending the first group.
   const int team = lane / L;
   const int tl = lane & (L - 1);
+  // the item this team takes within a warp's pass (TeamMap: keeps the two
+  // teams of an 8-lane phase on distinct shared-memory banks)
+  int titem = team;
+  if constexpr (TPW == 8) {
+    if (p.team_map == kTeamsApart4) {
+      titem = (team >> 1) + 4 * (team & 1);
+    } else if (p.team_map == kTeamsApart2) {
+      titem = (team & 4) + ((team >> 1) & 1) + 2 * (team & 1);
+    }
+  }
   const int nvec = static_cast<int>(Q * gs / SE);
   const int vb = static_cast<int>(gs / SE);
   const int items_per_pass = W * TPW;
@@ -454,7 +510,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     const unsigned char* sy = smem + static_cast<size_t>(2) * s * sb;
     const unsigned char* sg = sy + sb;
     for (int pass = 0; pass * items_per_pass < nitems; ++pass) {
-      const int item = pass * items_per_pass + warp * TPW + team;
+      const int item = pass * items_per_pass + warp * TPW + titem;
       const bool active = item < nitems;
       const int gl = item * Q;  // first group of the item within the unit
       int64_t out_off, wcol;    // output origin and weight column of that group
@@ -521,7 +577,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
           float r[SE];
           if (MODE == kMamba2) {
             float wv[SE];
-            load_w_cols<SE>(p, c, wcol + v * SE, wv);
+            load_w_cols<SE, kSwz>(p, c, wcol + v * SE, wv);
             mamba2_out<T, SE>(a[k], nlo, nhi, wv, r);
           } else {
             float sc[SE], gf[SE];

@@ -72,9 +72,10 @@ def test_workload_full_size_sampled(name):
 
 
 # group sizes: below, at and above the vector width, the warp width, the
-# register tile limits; odd spans
-GS_LIST = [1, 2, 3, 4, 6, 7, 8, 9, 10, 12, 16, 24, 31, 32, 33, 40, 50, 64, 100, 126, 127, 128, 129,
-           200, 250, 256,
+# register tile limits; odd spans; 72, 80, 112 (16-bit) put 4-lane streaming
+# teams on items 1, 2 and 6 shared-memory slots apart (each team map)
+GS_LIST = [1, 2, 3, 4, 6, 7, 8, 9, 10, 12, 16, 24, 31, 32, 33, 40, 50, 64, 72, 80, 100, 112, 126,
+           127, 128, 129, 200, 250, 256,
            264, 960, 1000, 1024, 1032, 2048, 4096, 5120, 5121, 8200]
 
 
