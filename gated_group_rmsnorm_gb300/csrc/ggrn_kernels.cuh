@@ -550,6 +550,19 @@ __global__ void __launch_bounds__(MAXT, wide_min_blocks(MODE, MAXT)) k_wide(cons
         gr[k] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // One vector per thread in CTAs of at most 256 threads (launches of a
+    // few groups, e.g. a decode step, where each group's latency is the
+    // cost): the weight is fetched with y and gate, not after the reduction,
+    // so its round trip overlaps theirs (decode 960-wide: 1.57 -> 1.47 us per
+    // call in a 21-call graph).  Not in the 1024-thread kernel: 9 more
+    // registers there halve the resident 640-thread CTAs (-23 % at 256 rows
+    // of 5120-wide groups).
+    constexpr bool kPrefetchW = VPL == 1 && MAXT <= 256;
+    float wpre[kPrefetchW ? E : 1];
+    if constexpr (kPrefetchW) {
+      if (tid < p.nvec)
+        load_weight_vec<T, MODE>(p.w, (MODE == kMamba2 ? col0 : 0) + (int64_t)tid * E, wpre);
+    }
     // MAMBA2: a = gated.  ONNX: a = x; the gate's raw words wait for the
     // epilogue (fewer live registers than its widened silu).
     float a[VPL][E];
@@ -584,11 +597,15 @@ __global__ void __launch_bounds__(MAXT, wide_min_blocks(MODE, MAXT)) k_wide(cons
       if (v < p.nvec) {
         float wv[E];
         uint4 o;
+        if constexpr (kPrefetchW) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) wv[e] = wpre[e];
+        } else {
+          load_weight_vec<T, MODE>(p.w, (MODE == kMamba2 ? col0 : 0) + (int64_t)v * E, wv);
+        }
         if (MODE == kMamba2) {
-          load_weight_vec<T, MODE>(p.w, col0 + (int64_t)v * E, wv);
           o = epilogue_mamba2<T>(a[k], nf, wv);
         } else {
-          load_weight_vec<T, MODE>(p.w, (int64_t)v * E, wv);
           float gf[E], sg[E];
           Elem<T>::unpack(gr[k], gf);
           silu_vec<T, E>(gf, sg);
