@@ -40,22 +40,30 @@ int64_t target_chunk_rows(int64_t rows, int64_t width, int es) {
 }
 
 // Row counts of the chunks, at most `t` each.  When there are enough rows,
-// the first two chunks are a quarter and a half of `t` and the last two
-// mirror them, so the copies of the two directions overlap sooner and longer
-// (+1-2 % end to end against equal chunks); the middle rows split evenly.
+// the first kRampLevels chunks grow geometrically to `t` (t/2^R, ..., t/2)
+// and the last ones mirror them, so the copies of the two directions overlap
+// sooner and longer (+1-2 % end to end against equal chunks at R = 2; deeper
+// ramps pay more per-copy fixed cost than they save: prefill 247.4 GB/s at
+// R = 2, 243 at R = 3-4, 240.7 at R = 5); the middle rows split evenly.
+constexpr int kRampLevels = 2;
 int64_t chunk_rows_at(int64_t rows, int64_t t, int64_t c, int64_t* n_chunks) {
-  const int64_t q = std::max<int64_t>(1, t / 4), h = std::max<int64_t>(1, t / 2);
-  if (rows <= 2 * (q + h) + t) {  // equal chunks
+  const int R = kRampLevels;
+  int64_t ramp[8], sum = 0;
+  for (int i = 0; i < R; ++i) {
+    ramp[i] = std::max<int64_t>(1, t >> (R - i));
+    sum += ramp[i];
+  }
+  if (rows <= 2 * sum + t) {  // equal chunks
     *n_chunks = (rows + t - 1) / t;
     return std::min(t, rows - c * t);
   }
-  const int64_t mid = rows - 2 * (q + h);
+  const int64_t mid = rows - 2 * sum;
   const int64_t k = (mid + t - 1) / t;  // middle chunks
   const int64_t m = (mid + k - 1) / k;
-  *n_chunks = k + 4;
-  if (c == 0 || c == k + 3) return q;
-  if (c == 1 || c == k + 2) return h;
-  return std::min(m, mid - (c - 2) * m);
+  *n_chunks = k + 2 * R;
+  if (c < R) return ramp[c];
+  if (c >= k + R) return ramp[k + 2 * R - 1 - c];
+  return std::min(m, mid - (c - R) * m);
 }
 
 // Streams and events of one device, created once (the first call there) and
