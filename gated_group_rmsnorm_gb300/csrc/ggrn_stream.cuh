@@ -462,10 +462,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     if (lane == 0) atomicOr(p.fault, kFaultConsumerWait);
     return;
   }
-  // (for teams of 8+ lanes, whose 8-lane phases read consecutive blocks;
-  // narrower teams read the weight at scattered columns: on the paired
-  // 4-lane teams of the odd span the permutation measured 0.35 % slower)
-  constexpr bool kSwz = MODE == kMamba2 && SE == 8 && Q == 1 && L >= 8;
+  // (teams of 8+ lanes, whose 8-lane phases read consecutive blocks; and
+  // paired 4-lane teams, whose phases hold two items 4 apart under the
+  // planner's kTeamsApart4 map: their blocks are 100 apart for the 200-wide
+  // pairs of 100-wide bf16 groups, and adding 100 flips bit 2)
+  constexpr bool kSwz = MODE == kMamba2 && SE == 8 && ((Q == 1 && L >= 8) || (Q == 2 && L == 4));
   if (kSwz && wbytes) {
     // permute the staged weight (all consumer threads), then wait until
     // every consumer thread has finished its share (bounded like every wait)
