@@ -94,7 +94,9 @@ constexpr int kStreamWarps = 8;  // consumer warps per CTA (target)
 constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of one SM share
 // Ring stages (at most; the shared-memory budget may allow fewer).
 constexpr int64_t kStreamMaxStages = 2;
-constexpr int64_t kStreamMinUnitsPerSlot = 12;
+constexpr int64_t kStreamMinUnitsPerSlot = 12;        // units per CTA slot to stream (see plan_stream)
+constexpr int64_t kStreamMinUnitsPerSlotNarrow = 36;  // teams of at most 4 lanes, one group each
+constexpr int64_t kStreamMinUnitsPerSlotPaired = 8;   // paired 4 x 7 teams
 constexpr int64_t kStreamMaxWeightBytes = 64 * 1024;
 
 int elem_size(int dtype) { return dtype == kF32 ? 4 : 2; }
@@ -391,7 +393,7 @@ int64_t stream_head_size(int mode, int64_t mid, int Q) {
 // Q = 2 when they are an odd multiple of 8 (a pair of groups is then whole
 // 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
 // vectors, every unit is a 16-byte multiple, and (unless forced) there are
-// at least kStreamMinUnitsPerSlot units per CTA slot.
+// enough units per CTA slot (kStreamMinUnitsPerSlot and its variants).
 int plan_stream(const Args& a, Plan* p, bool forced) {
   const int es = elem_size(a.dtype);
   const int64_t gbytes = a.gs * es;
@@ -481,11 +483,18 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   if (!stream_smem(stage_bytes, wb, max_stages, &cps, &ns, &wstage))
     return GGRN_ERR_UNSUPPORTED;
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
-  // Automatic selection streams only with 12+ units per CTA slot: below that
-  // the ring's fill and drain cost more than the register-resident TEAM
-  // kernel loses (measured crossovers: about 13 units per slot on the
-  // 960-wide prefill groups, 18 on 128-wide heads, 11 on the odd span).
-  if (!forced && units < kStreamMinUnitsPerSlot * gmax) return GGRN_ERR_UNSUPPORTED;
+  // Automatic selection streams only with enough units per CTA slot: below
+  // that the ring's fill and drain cost more than the register-resident TEAM
+  // kernel loses.  Measured crossovers (TEAM vs STREAM, GB/s): 960-wide
+  // prefill groups, 32-lane teams, 12 per slot (3072 rows 5824 vs 5525, 4096
+  // rows 6068 vs 6101); 128-wide fp16 heads, 4-lane teams, 36 per slot (8192
+  // rows 6355 vs 6248, 16384 rows 6790 vs 6800, 24576 rows 6923 vs 7002);
+  // the odd span's paired 4 x 7 teams, 8 per slot (5120 rows 4799 vs 4772,
+  // 6144 rows 4989 vs 5025, 8192 rows 5156 vs 5398).
+  int64_t min_per_slot = kStreamMinUnitsPerSlot;
+  if (Q == 1 && lanes <= 4) min_per_slot = kStreamMinUnitsPerSlotNarrow;
+  if (Q == 2 && vpl == 7) min_per_slot = kStreamMinUnitsPerSlotPaired;
+  if (!forced && units < min_per_slot * gmax) return GGRN_ERR_UNSUPPORTED;
   // static schedule: equal units per CTA, so the last wave ends together
   const int64_t per_cta = ceil_div(units, gmax);
   p->path = kStream;

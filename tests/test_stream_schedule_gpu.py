@@ -36,10 +36,11 @@ def _fwd(wl, dev, out=None):
                      out=out, path=g.PATH_STREAM)
 
 
-# rows at which automatic selection streams (12+ units per CTA slot), so that
-# the library's own graph API, which selects automatically, records STREAM too
-@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 4096), ("gdn_onnx", 5600),
-                                       ("strided_odd_span", 9200)])
+# rows at which automatic selection streams (12, 36 and 8 units per CTA slot
+# for these three team layouts), so that the library's own graph API, which
+# selects automatically, records STREAM too
+@pytest.mark.parametrize("name,rows", [("mamba2_prefill", 4096), ("gdn_onnx", 16800),
+                                       ("strided_odd_span", 6400)])
 def test_claimed_schedule_matches_oracle_and_graph_replay(name, rows):
     g.fault_status(clear=True)
     wl, host, dev = _case(name, rows)
