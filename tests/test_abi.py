@@ -270,3 +270,18 @@ def test_stream_short_first_units():
     # chunk units (part of a row each) keep one size
     p = _plan(4096, 3 * 4096, 4096 // 4, 2, ys=4 * 4096, path=g.PATH_STREAM)
     assert p.items % 4096 == 0
+
+
+def test_stream_threshold_by_team_layout():
+    """Automatic selection streams from 12 units per CTA slot for 32-lane
+    teams, 36 for teams of at most 4 lanes and 8 for paired 4 x 7 teams."""
+    # prefill: 2-row units, 152 slots -> from 12 * 152 units (3647 rows)
+    assert _plan(3645, 7680, 960, 2).path != g.PATH_STREAM
+    assert _plan(3648, 7680, 960, 2).path == g.PATH_STREAM
+    # 128-wide fp16 heads: units of 48 of the 32 heads a row, 304 slots ->
+    # from 36 * 304 units (16415 rows)
+    assert _plan(16413, 4096, 128, 1, mode=1).path == g.PATH_TEAM
+    assert _plan(16416, 4096, 128, 1, mode=1).path == g.PATH_STREAM
+    # odd span: 5-row units, 152 slots -> from 8 * 152 units (6076 rows)
+    assert _plan(6075, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
+    assert _plan(6080, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
