@@ -68,12 +68,18 @@ struct Plan {
 };
 
 // Most consumer warps of a streaming launch (the kernels' launch bounds).
-// 4-lane x 7-vector paired items fit 96 registers in MAMBA2 mode (16 warps);
-// in ONNX mode they also keep the gate's words, and 12 warps leave 128.
+// Each SM sub-partition holds a quarter of the register file, so a CTA of
+// 17 warps (5 on one sub-partition) leaves 96 registers a thread, one of
+// 16 or fewer leaves 128.  The 4-lane x 7-vector paired kernel is launched
+// with 15 consumer warps in MAMBA2 mode (the odd span), where 128 registers
+// remove its spills; in ONNX mode it also keeps the gate's words, and 12
+// warps leave 128 as well.
 constexpr int kStreamMaxWarps = 16;
+constexpr int kStreamMaxWarps4x7 = 15;
 constexpr int kStreamMaxWarps4x7Onnx = 12;
 constexpr int stream_max_warps(int mode, int vpl) {
-  return (vpl == 7 && mode == kOnnx) ? kStreamMaxWarps4x7Onnx : kStreamMaxWarps;
+  return vpl == 7 ? (mode == kOnnx ? kStreamMaxWarps4x7Onnx : kStreamMaxWarps4x7)
+                  : kStreamMaxWarps;
 }
 
 // Kernel parameters (passed by value).
