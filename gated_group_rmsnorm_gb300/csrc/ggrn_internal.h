@@ -70,16 +70,14 @@ struct Plan {
 // Most consumer warps of a streaming launch (the kernels' launch bounds).
 // Each SM sub-partition holds a quarter of the register file, so a CTA of
 // 17 warps (5 on one sub-partition) leaves 96 registers a thread, one of
-// 16 or fewer leaves 128.  The 4-lane x 7-vector paired kernel is launched
-// with 15 consumer warps in MAMBA2 mode (the odd span), where 128 registers
-// remove its spills; in ONNX mode it also keeps the gate's words, and 12
-// warps leave 128 as well.
+// 16 or fewer leaves 128.  The 4-lane x 7-vector paired kernel is bound at
+// 15 consumer warps (+ the producer: 16), where 128 registers hold it
+// without spills in both modes (ONNX also keeps the gate's words).
 constexpr int kStreamMaxWarps = 16;
 constexpr int kStreamMaxWarps4x7 = 15;
-constexpr int kStreamMaxWarps4x7Onnx = 12;
 constexpr int stream_max_warps(int mode, int vpl) {
-  return vpl == 7 ? (mode == kOnnx ? kStreamMaxWarps4x7Onnx : kStreamMaxWarps4x7)
-                  : kStreamMaxWarps;
+  (void)mode;
+  return vpl == 7 ? kStreamMaxWarps4x7 : kStreamMaxWarps;
 }
 
 // Kernel parameters (passed by value).
