@@ -587,7 +587,17 @@ __global__ void __launch_bounds__(MAXT, wide_min_blocks(MODE, MAXT)) k_wide(cons
     if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
     __syncthreads();
     float m2 = 0.0f;
-    for (int i = 0; i < nwarps; ++i) m2 += red[parity][i];
+    if (MAXT > 256 && nwarps > 8) {
+      // many warps (a single wide group, e.g. batch-1 decode of one
+      // 7680-wide group): one shared-memory read per lane and a butterfly,
+      // instead of a chain of nwarps dependent reads; the xor butterfly adds
+      // each pair symmetrically, so every lane ends with the same bits
+      m2 = (tid & 31) < nwarps ? red[parity][tid & 31] : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+    } else {
+      for (int i = 0; i < nwarps; ++i) m2 += red[parity][i];
+    }
     const float nf = normaliser(m2, p.gs_f, p.eps);
 
     T* op = static_cast<T*>(p.out) + row * p.os + col0;
