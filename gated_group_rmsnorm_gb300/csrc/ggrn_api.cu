@@ -273,10 +273,16 @@ int plan_wide(const Args& a, Plan* p, int vpl = kWideVpl) {
 
 // Vectors per thread of WIDE: 1 up to two groups per SM, 2 up to four, then
 // 4, as the CTA size limit allows (5120-wide groups: at 256 rows 1 vector per
-// thread 1.98 TB/s against 1.57 with 4; at 1024 rows 4 is best).
+// thread 1.98 TB/s against 1.57 with 4; at 1024 rows 4 is best).  One vector
+// per thread stops at 640 threads: a lone 7680-wide group (batch-1 decode
+// with one group) takes 2.34 us per call in a 21-call graph with 480 threads
+// of 2 vectors against 2.59 with 960 of 1, while a lone 5120-wide group is
+// faster with 640 threads of 1 (2.05 against 2.15).
+constexpr int64_t kWideOneVecMaxThreads = 640;
 int wide_vpl(const Args& a, int64_t items, int64_t sms) {
   const int64_t nvec = a.gs / (16 / elem_size(a.dtype));
   int v = items <= 2 * sms ? 1 : (items <= 4 * sms ? 2 : 4);
+  if (v == 1 && nvec > kWideOneVecMaxThreads) v = 2;
   while (v < 4 && ceil_div(nvec, v) > kWideMaxThreads) v *= 2;
   return v;
 }
