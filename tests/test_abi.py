@@ -285,3 +285,44 @@ def test_stream_threshold_by_team_layout():
     # odd span: 5-row units, 152 slots -> from 8 * 152 units (6076 rows)
     assert _plan(6075, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
     assert _plan(6080, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
+
+
+def test_plans_respect_launch_limits():
+    """A seeded sweep of shapes, strides, dtypes, modes and forced families:
+    every plan the host accepts is a launch the device accepts (block and
+    shared-memory limits, the streaming kernels' warp bounds, a nonempty
+    grid), and a refusal is one of the documented statuses."""
+    import random
+    rnd = random.Random(1234)
+    gs_pool = [1, 3, 4, 8, 12, 16, 24, 40, 64, 72, 80, 96, 100, 112, 128, 200, 256, 384, 960,
+               1000, 1024, 2048, 4096, 5120, 7680, 8200]
+    allowed = {binding.ERR_UNSUPPORTED, binding.ERR_ALIGN}
+    checked = 0
+    for _ in range(1500):
+        dtype = rnd.choice((0, 1, 2))
+        mode = rnd.choice((0, 1)) if dtype != 2 else 0
+        gs = rnd.choice(gs_pool)
+        width = gs * rnd.choice((1, 2, 3, 8, 32, 48))
+        if width > 1 << 16:
+            continue
+        rows = rnd.choice((1, 2, 7, 64, 1000, 4096, 20000, 70000))
+        ys = width + rnd.choice((0, 0, 8, 64))
+        path = rnd.choice((0, 0, 1, 2, 3, 4, 5))
+        st, info = g.ggrn_plan(1 << 40, 2 << 40, 3 << 40, 0, rows, width, gs, ys, ys, width, dtype,
+                               mode, path)
+        if st != binding.OK:
+            assert path != 0 and st in allowed, (st, rows, width, gs, ys, dtype, mode, path)
+            continue
+        checked += 1
+        case = (rows, width, gs, ys, dtype, mode, path, info.as_dict())
+        assert info.grid_blocks >= 1 and info.items >= 1, case
+        assert 32 <= info.block_threads <= 1024 and info.block_threads % 32 == 0, case
+        assert 0 <= info.smem_bytes <= 227 * 1024, case
+        if info.path == g.PATH_STREAM:
+            bound = 16 if info.vec_per_lane == 7 else 17   # consumer warps + producer
+            assert info.block_threads <= bound * 32, case
+            assert info.smem_bytes > 0, case
+        if path == 0:
+            assert info.path in (g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR,
+                                 g.PATH_STREAM), case
+    assert checked > 500
