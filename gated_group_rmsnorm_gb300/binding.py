@@ -323,13 +323,15 @@ def host_workspace(rows: int, width: int, dtype, device) -> torch.Tensor:
 def forward_host(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_size: int,
                  eps: float, mode="mamba2", out: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """The operation on CPU tensors, copies and kernels overlapped
-    (``ggrn_forward_host``), enqueued on the current stream of ``w``'s device.
+    """The operation on CPU tensors (``ggrn_forward_host``), enqueued on the
+    current stream of ``w``'s device.  Pinned y, gate and out are read and
+    written in place by the kernel over the host link; other host memory is
+    staged through a device workspace with the copies overlapped.
 
-    ``y``, ``gate``: CPU [..., width] tensors (pinned for the copies to
-    overlap).  ``w``: the weight / scale on the GPU.  ``out``: optional CPU
-    output (allocated pinned when omitted).  ``workspace``: optional device
-    uint8 tensor (``host_workspace`` when omitted).  The result is complete
+    ``y``, ``gate``: CPU [..., width] tensors.  ``w``: the weight / scale on
+    the GPU.  ``out``: optional CPU output (allocated pinned when omitted).
+    ``workspace``: optional device uint8 tensor for the copy route
+    (``host_workspace`` when omitted and needed).  The result is complete
     when the stream reaches this point (synchronise before reading it).
     """
     if y.is_cuda or gate.is_cuda:
@@ -350,13 +352,14 @@ def forward_host(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_
     rows, ys = _as_rows(y, width, "y")
     _, gts = _as_rows(gate, width, "gate")
     _, os_ = _as_rows(out, width, "out")
-    if workspace is None:
+    if workspace is None and not (y.is_pinned() and gate.is_pinned() and out.is_pinned()):
         workspace = host_workspace(rows, width, y.dtype, w.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     with torch.cuda.device(w.device):
         st = ggrn_forward_host(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows,
                                width, group_size, ys, gts, os_, float(eps), DTYPE_CODE[y.dtype], m,
-                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                               _stream_handle(w.device))
+                               ws_ptr, ws_bytes, _stream_handle(w.device))
     if st != OK:
         raise GgrnError(st, "ggrn_forward_host")
     return out

@@ -146,32 +146,40 @@ int ggrn_forward_inproj(const void* inproj, int64_t inproj_row_stride, int64_t y
                         int mode, void* cuda_stream);
 
 /*
- * ggrn_forward_host -- the operation on HOST-resident y, gate and out, with
- * the host<->device copies overlapped with the kernels.  Rows are cut into
- * chunks that cycle through three slots of `workspace`; on three streams of
- * the library (created on the first call on a device), the host-to-device
- * copies of one chunk, the kernel of the previous one and the
- * device-to-host copy of the one before run at the same time.  Ordered
- * after the work already on `cuda_stream`; work enqueued on `cuda_stream`
- * afterwards runs after the last output row has arrived in `out_host`.
+ * ggrn_forward_host -- the operation on HOST-resident y, gate and out.
+ * Two routes, chosen per call:
+ *   - y_host, gate_host and out_host all mapped into the current device's
+ *     address space at their own addresses (page-locked memory from
+ *     cudaHostAlloc/cudaMallocHost, or registered with cudaHostRegister, on
+ *     a system with unified addressing): one kernel on `cuda_stream` reads y
+ *     and gate and writes out in place over the host link (plain loads and
+ *     stores; no copies, the workspace unused and allowed to be NULL);
+ *   - otherwise rows are cut into chunks that cycle through three slots of
+ *     `workspace`; on three streams of the library (created on the first
+ *     call on a device), the host-to-device copies of one chunk, the kernel
+ *     of the previous one and the device-to-host copy of the one before run
+ *     at the same time.
+ * Either way ordered after the work already on `cuda_stream`; work enqueued
+ * on `cuda_stream` afterwards runs after the last output row has arrived in
+ * `out_host`.
  *   y_host, gate_host : const T*, host [rows, width] matrices with the given
- *                       row strides (elements).  Pinned (page-locked) memory
- *                       is needed for the copies to overlap; pageable memory
- *                       gives correct results with the copies serialised.
+ *                       row strides (elements).  Pageable memory gives
+ *                       correct results with the copies serialised.
  *   out_host          : T*, host, row stride out_row_stride.
  *   w                 : DEVICE pointer, as in ggrn_forward.
  *   workspace         : DEVICE memory owned by the caller, 16-byte aligned,
- *                       workspace_bytes long; ggrn_host_workspace_bytes()
- *                       gives the size that allows full-size chunks; less
- *                       shortens the chunks (at least one row per slot:
- *                       9 x (width x sizeof(T) rounded up to 256) bytes).
+ *                       workspace_bytes long (copy route only);
+ *                       ggrn_host_workspace_bytes() gives the size that
+ *                       allows full-size chunks; less shortens the chunks (at
+ *                       least one row per slot: 9 x (width x sizeof(T)
+ *                       rounded up to 256) bytes).
  *   other arguments   : as in ggrn_forward.
  * Returns the ggrn_forward statuses (argument checks on the host matrices,
- * before anything is enqueued), GGRN_ERR_NULL for a NULL workspace,
- * GGRN_ERR_ALIGN for a misaligned one, GGRN_ERR_ARG for one too small.
- * Calls from several host threads on one device are serialised while they
- * enqueue; the workspace of a call must not be used by other work until
- * `cuda_stream` has passed the call.
+ * before anything is enqueued); on the copy route also GGRN_ERR_NULL for a
+ * NULL workspace, GGRN_ERR_ALIGN for a misaligned one, GGRN_ERR_ARG for one
+ * too small.  Calls from several host threads on one device are serialised
+ * while they enqueue; the workspace of a call must not be used by other work
+ * until `cuda_stream` has passed the call.
  */
 int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w, void* out_host,
                       int64_t rows, int64_t width, int64_t group_size, int64_t y_row_stride,

@@ -1,7 +1,9 @@
-"""ggrn_forward_host: host-resident y, gate and out, the copies overlapped
-with the kernels (GPU).  Every output row must arrive, match the oracle,
-and match the device-resident call within the parity tolerance (chunks may
-take another kernel family than the whole call)."""
+"""ggrn_forward_host: host-resident y, gate and out (GPU).  Pinned buffers
+are read and written in place by one kernel over the host link; pageable
+ones go through the workspace with the copies overlapped.  On both routes
+every output row must arrive, match the oracle, and match the
+device-resident call within the parity tolerance (the routes and the chunks
+may take another kernel family than the whole device call)."""
 import pytest
 import torch
 
@@ -32,11 +34,12 @@ def _host_case(name, rows, pinned=True, seed=0):
     return wl, inp, y, gate
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["in_place", "copies"])
 @pytest.mark.parametrize("name,rows", [("mamba2_prefill", 1031), ("gdn_onnx", 2048),
                                        ("strided_odd_span", 777), ("wide_single_group", 300),
                                        ("mamba2_decode", 1)])
-def test_matches_oracle_and_device_call(name, rows):
-    wl, inp, y, gate = _host_case(name, rows)
+def test_matches_oracle_and_device_call(name, rows, pinned):
+    wl, inp, y, gate = _host_case(name, rows, pinned=pinned)
     w = inp.w.cuda()
     out = g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
     torch.cuda.synchronize()
@@ -44,7 +47,10 @@ def test_matches_oracle_and_device_call(name, rows):
     res = gpu_util.compare(out, inp, wl.group_size, wl.eps, wl.mode)
     assert res["ok"], res
     dev = g.forward(y.cuda(), gate.cuda(), w, group_size=wl.group_size, eps=wl.eps, mode=wl.mode)
-    assert int(ulp_dist(out, dev.cpu()).max()) <= 1
+    # the two calls may sum in different orders (other families): in MAMBA2
+    # mode a flip of the intermediate cast becomes up to 2 ulp after the
+    # weight's rounding, the case the tolerance against the oracle admits
+    assert int(ulp_dist(out, dev.cpu()).max()) <= (2 if wl.mode == 0 else 1)
 
 
 def test_small_workspace_pageable_memory_and_reuse():
@@ -80,13 +86,16 @@ def test_ordered_on_the_callers_stream():
     assert not bool((out == -1280.0).any())
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["in_place", "copies"])
 @pytest.mark.parametrize("pw,ycol,gcol", [(9664, 64, 4864),    # joint copy, y not at row start
                                           (9664, 4864, 0),     # joint copy, gate first
                                           (14400, 0, 9600)])   # too much unused: 2-D copies
-def test_packed_host_buffers(pw, ycol, gcol):
+def test_packed_host_buffers(pw, ycol, gcol, pinned):
     rows, width, gs = 333, 4800, 100
     gen = torch.Generator().manual_seed(pw + ycol)
-    packed = torch.randn(rows, pw, generator=gen).to(torch.bfloat16).pin_memory()
+    packed = torch.randn(rows, pw, generator=gen).to(torch.bfloat16)
+    if pinned:
+        packed = packed.pin_memory()
     w = 1.0 + 0.1 * torch.randn(width, generator=gen)
     y, gate = packed[:, ycol:ycol + width], packed[:, gcol:gcol + width]
     ws = g.host_workspace(rows, width, torch.bfloat16, "cuda")
@@ -95,3 +104,24 @@ def test_packed_host_buffers(pw, ycol, gcol):
     host = ggrn_inputs.Inputs(y=y.contiguous(), gate=gate.contiguous(), w=w)
     res = gpu_util.compare(out, host, gs, 1e-5, 0)
     assert res["ok"], res
+
+
+def test_route_by_host_memory():
+    """Pinned y, gate and out are read in place: the workspace is left as it
+    was (and may be omitted); pageable ones are staged through it."""
+    wl, inp, y, gate = _host_case("mamba2_prefill", 300, seed=8)
+    w = inp.w.cuda()
+    ws = torch.full((g.host_workspace(300, wl.width, wl.dtype, "cuda").numel(),), 0x5A,
+                    dtype=torch.uint8, device="cuda")
+    out = g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((ws == 0x5A).all()), "pinned buffers went through the workspace"
+    assert gpu_util.compare(out, inp, wl.group_size, wl.eps, wl.mode)["ok"]
+    out2 = g.forward_host(y, gate, w, group_size=wl.group_size, eps=wl.eps)  # no workspace
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    out3 = g.forward_host(y.clone(), gate.clone(), w, group_size=wl.group_size, eps=wl.eps,
+                          out=torch.empty(y.shape, dtype=y.dtype), workspace=ws)
+    torch.cuda.synchronize()
+    assert not bool((ws == 0x5A).all()), "pageable buffers did not use the workspace"
+    assert gpu_util.compare(out3, inp, wl.group_size, wl.eps, wl.mode)["ok"]
