@@ -125,3 +125,21 @@ def test_route_by_host_memory():
     torch.cuda.synchronize()
     assert not bool((ws == 0x5A).all()), "pageable buffers did not use the workspace"
     assert gpu_util.compare(out3, inp, wl.group_size, wl.eps, wl.mode)["ok"]
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["in_place", "copies"])
+def test_misaligned_host_views(pinned):
+    """y and gate one element off a 16-byte boundary (element loads only) and
+    an odd row stride: still correct on both routes."""
+    rows, width, gs = 129, 960, 96
+    gen = torch.Generator().manual_seed(21)
+    buf = torch.randn(rows, 2 * width + 3, generator=gen).to(torch.bfloat16)
+    if pinned:
+        buf = buf.pin_memory()
+    y, gate = buf[:, 1:1 + width], buf[:, 2 + width:2 + 2 * width]
+    w = 1.0 + 0.1 * torch.randn(width, generator=gen)
+    out = g.forward_host(y, gate, w.cuda(), group_size=gs, eps=1e-5)
+    torch.cuda.synchronize()
+    host = ggrn_inputs.Inputs(y=y.contiguous(), gate=gate.contiguous(), w=w)
+    res = gpu_util.compare(out, host, gs, 1e-5, 0)
+    assert res["ok"], res
