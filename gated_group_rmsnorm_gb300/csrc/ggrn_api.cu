@@ -614,27 +614,6 @@ int make_plan(const Args& a, int path, Plan* p) {
   }
 }
 
-// Kernels that read y and gate and write out in host memory mapped into the
-// device's address space (pinned host memory reached over the host link):
-// plain loads and stores only, never STREAM's bulk copies, and the family
-// that measured fastest over the link.  Pinned host buffers, GB/s (WIDE /
-// TEAM / STRADDLE): prefill 960-wide groups 284 / 278 / -; 5120-wide groups
-// 289 / - / -; 128-wide fp16 heads 304 / 267 / -; the odd span's 100-wide
-// groups read in place from the packed buffer - / 223 / 284.
-int make_plan_in_place(const Args& a, Plan* p) {
-  *p = Plan();
-  if (vector_layout_ok(a)) {
-    const int64_t items = a.rows * (a.width / a.gs);
-    if (plan_wide(a, p, wide_vpl(a, items, sm_count())) == GGRN_OK) return GGRN_OK;
-    *p = Plan();
-    if (plan_straddle(a, p) == GGRN_OK) return GGRN_OK;
-    *p = Plan();
-    if (plan_team(a, p) == GGRN_OK) return GGRN_OK;
-    *p = Plan();
-  }
-  return plan_scalar(a, p);
-}
-
 Args make_args(const void* y, const void* gate, const void* w, void* out, int64_t rows,
                int64_t width, int64_t gs, int64_t ys, int64_t gts, int64_t os, float eps,
                int dtype, int mode) {
@@ -724,14 +703,24 @@ int validate_call(const Args& a) { return validate(a); }
 
 int forward_call(const Args& a, cudaStream_t s) { return forward_impl(a, kAuto, s); }
 
-int forward_call_in_place(const Args& a, cudaStream_t s) {
-  int st = validate(a);
-  if (st != GGRN_OK || a.rows == 0) return st;
-  Plan p;
-  st = make_plan_in_place(a, &p);
-  if (st != GGRN_OK) return st;
-  return launch(a, p, s);
+int plan_family(const Args& a, int path, int vpl, Plan* p) {
+  *p = Plan();
+  switch (path) {
+    case kTeam:
+    case kWide:
+    case kStraddle:
+      if (!vector_layout_ok(a)) return GGRN_ERR_ALIGN;
+      if (path == kTeam) return plan_team(a, p);
+      if (path == kWide) return plan_wide(a, p, vpl);
+      return plan_straddle(a, p);
+    case kScalar:
+      return plan_scalar(a, p);
+    default:
+      return GGRN_ERR_ARG;
+  }
 }
+
+int launch_plan(const Args& a, const Plan& p, cudaStream_t s) { return launch(a, p, s); }
 
 void record_cuda_error(cudaError_t e) { tl_last_cuda_error = e; }
 

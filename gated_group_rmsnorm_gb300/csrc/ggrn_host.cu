@@ -80,6 +80,29 @@ bool device_maps_in_place(const void* p) {
   return at.type == cudaMemoryTypeHost && at.devicePointer == p;
 }
 
+// Kernels that read y and gate and write out in host memory mapped into the
+// device's address space (pinned host memory reached over the host link):
+// plain loads and stores only, never STREAM's bulk copies, and the family
+// that measured fastest over the link.  Pinned host buffers, GB/s (WIDE /
+// TEAM / STRADDLE): prefill 960-wide groups 284 / 278 / -; 5120-wide groups
+// 289 / - / -; 128-wide fp16 heads 304 / 267 / -; the odd span's 100-wide
+// groups read in place from the packed buffer - / 223 / 284.  WIDE with one
+// vector per thread (more requests in flight per group) did better still:
+// prefill 296 (4 vectors: 282), 5120-wide 302 (289), heads 303 (303).
+int forward_in_place(const Args& a, cudaStream_t s) {
+  const int64_t nvec = a.gs / (16 / es_of(a.dtype));
+  int vpl = 1;
+  while (vpl < 4 && (nvec + vpl - 1) / vpl > 1024) vpl *= 2;
+  Plan p;
+  int st = GGRN_ERR_UNSUPPORTED;
+  for (const int path : {kWide, kStraddle, kTeam, kScalar}) {
+    st = plan_family(a, path, vpl, &p);
+    if (st == GGRN_OK) break;
+  }
+  if (st != GGRN_OK) return st;
+  return launch_plan(a, p, s);
+}
+
 // Both ends of a [rows, width] matrix of es-byte elements at row stride
 // `stride` elements (a matrix that runs past its page-locked allocation
 // takes the copy route).
@@ -164,7 +187,7 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
   if (matrix_maps_in_place(y_host, rows, width, a.ys, es) &&
       matrix_maps_in_place(gate_host, rows, width, a.gts, es) &&
       matrix_maps_in_place(out_host, rows, width, a.os, es))
-    return forward_call_in_place(a, static_cast<cudaStream_t>(cuda_stream));
+    return forward_in_place(a, static_cast<cudaStream_t>(cuda_stream));
   if (!workspace) return GGRN_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return GGRN_ERR_ALIGN;
   const int64_t row_bytes = width * es;

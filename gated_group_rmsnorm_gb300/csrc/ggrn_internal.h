@@ -135,9 +135,11 @@ Args call_args(const void* y, const void* gate, const void* w, void* out, int64_
                int dtype, int mode);
 int validate_call(const Args& a);
 int forward_call(const Args& a, cudaStream_t s);
-// As forward_call, for y, gate and out in host memory the device reaches in
-// place (mapped at the same address): plain-load families only.
-int forward_call_in_place(const Args& a, cudaStream_t s);
+// One plain-load family planned for validated arguments (kTeam, kWide with
+// `vpl` vectors per thread, kStraddle, kScalar): GGRN_OK, or the status that
+// refuses it; and the launch of a plan on a stream.
+int plan_family(const Args& a, int path, int vpl, Plan* p);
+int launch_plan(const Args& a, const Plan& p, cudaStream_t s);
 // Remember the CUDA error behind a GGRN_ERR_CUDA (ggrn_last_cuda_error).
 void record_cuda_error(cudaError_t e);
 
