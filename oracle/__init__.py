@@ -79,6 +79,9 @@ class Oracle:
         L.ggrn_oracle_forward_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                              f, ci, ci]
         L.ggrn_oracle_forward_ex.restype = ci
+        L.ggrn_oracle_forward_pre.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                              i64, f, ci, ci]
+        L.ggrn_oracle_forward_pre.restype = ci
         L.ggrn_oracle_encode.argtypes = [vp, vp, i64, ci]
         L.ggrn_oracle_encode.restype = None
         L.ggrn_oracle_decode.argtypes = [vp, vp, i64, ci]
@@ -117,6 +120,31 @@ class Oracle:
         if st != 0:
             raise OracleError(st)
         return (out, t_out) if want_t else out
+
+    def forward_detail(self, y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *,
+                       group_size: int, eps: float, mode: int = MAMBA2):
+        """Run the oracle and also return what the comparison rules need.
+
+        Returns ``(out, t, pre)``: ``out`` as ``forward``; ``t`` the MAMBA2
+        intermediate cast_T(gated*nf) (None in ONNX mode); ``pre`` f32
+        [rows, width], each element's value just before its rounding to T
+        (MAMBA2: gated*nf; ONNX: the product the store rounds).
+        """
+        for t in (y, gate, w):
+            assert t.device.type == "cpu"
+        rows, width = y.shape
+        out = torch.empty((rows, width), dtype=y.dtype)
+        t_out = torch.empty((rows, width), dtype=y.dtype) if mode == MAMBA2 else None
+        pre = torch.empty((rows, width), dtype=torch.float32)
+        w = w.contiguous()
+        st = self.lib.ggrn_oracle_forward_pre(
+            y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(),
+            t_out.data_ptr() if t_out is not None else None, pre.data_ptr(), rows, width,
+            group_size, _row_stride(y, width), _row_stride(gate, width), width, float(eps),
+            DTYPE_CODE[y.dtype], mode)
+        if st != 0:
+            raise OracleError(st)
+        return out, t_out, pre
 
     def status(self, y_ptr, gate_ptr, w_ptr, out_ptr, rows, width, group_size, ys, gs_, os_,
                eps, dtype, mode) -> int:

@@ -168,12 +168,12 @@ int validate(const void* y, const void* gate, const void* w, const void* out,
 
 }  // namespace
 
-extern "C" int ggrn_oracle_forward_ex(const void* y, const void* gate, const void* w,
-                                      void* out, void* t_out, int64_t rows,
-                                      int64_t width, int64_t group_size,
-                                      int64_t y_row_stride, int64_t gate_row_stride,
-                                      int64_t out_row_stride, float eps, int dtype,
-                                      int mode) {
+extern "C" int ggrn_oracle_forward_pre(const void* y, const void* gate, const void* w,
+                                       void* out, void* t_out, float* pre_out, int64_t rows,
+                                       int64_t width, int64_t group_size,
+                                       int64_t y_row_stride, int64_t gate_row_stride,
+                                       int64_t out_row_stride, float eps, int dtype,
+                                       int mode) {
   int st = validate(y, gate, w, out, rows, width, group_size, y_row_stride,
                     gate_row_stride, out_row_stride, dtype, mode);
   if (st != GGRN_ORACLE_OK || rows == 0) return st;
@@ -217,7 +217,9 @@ extern "C" int ggrn_oracle_forward_ex(const void* y, const void* gate, const voi
         const int64_t col = col0 + j;
         if (mode == GGRN_ORACLE_MODE_MAMBA2) {
           // out = cast(f32(w[col]) * f32(cast(gated * nf, T)), T)
-          float t = round_to_t(gated[j] * nf, dtype);
+          const float pre = gated[j] * nf;
+          if (pre_out) pre_out[n * width + col] = pre;
+          float t = round_to_t(pre, dtype);
           if (t_out) store_elem(t_out, n * width + col, t, dtype);
           float p = static_cast<const float*>(w)[col] * t;
           store_elem(out, n * out_row_stride + col, p, dtype);
@@ -228,12 +230,24 @@ extern "C" int ggrn_oracle_forward_ex(const void* y, const void* gate, const voi
           float r = x[j] * nf;
           r = r * s;
           r = r * silu_f32(b);
+          if (pre_out) pre_out[n * width + col] = r;
           store_elem(out, n * out_row_stride + col, r, dtype);
         }
       }
     }
   }
   return GGRN_ORACLE_OK;
+}
+
+extern "C" int ggrn_oracle_forward_ex(const void* y, const void* gate, const void* w,
+                                      void* out, void* t_out, int64_t rows,
+                                      int64_t width, int64_t group_size,
+                                      int64_t y_row_stride, int64_t gate_row_stride,
+                                      int64_t out_row_stride, float eps, int dtype,
+                                      int mode) {
+  return ggrn_oracle_forward_pre(y, gate, w, out, t_out, nullptr, rows, width, group_size,
+                                 y_row_stride, gate_row_stride, out_row_stride, eps, dtype,
+                                 mode);
 }
 
 extern "C" int ggrn_oracle_forward(const void* y, const void* gate, const void* w, void* out,

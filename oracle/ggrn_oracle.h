@@ -75,6 +75,18 @@ int ggrn_oracle_forward_ex(const void* y, const void* gate, const void* w, void*
                            int64_t gate_row_stride, int64_t out_row_stride,
                            float eps, int dtype, int mode);
 
+/* As ggrn_oracle_forward_ex, and pre_out (optional, contiguous [rows, width]
+ * f32) receives each element's value just before its rounding to T: MAMBA2
+ * the product gated * nf that the intermediate cast rounds, ONNX the product
+ * that the store rounds.  The comparison rules of the tests use it to tell
+ * whether a one-ulp difference of the intermediate (a "flip" caused by a
+ * different summation order) can explain a difference of the output. */
+int ggrn_oracle_forward_pre(const void* y, const void* gate, const void* w, void* out,
+                            void* t_out, float* pre_out, int64_t rows, int64_t width,
+                            int64_t group_size, int64_t y_row_stride,
+                            int64_t gate_row_stride, int64_t out_row_stride,
+                            float eps, int dtype, int mode);
+
 /* Same definition evaluated in double; only the casts to T round
  * (directly from double, RNE).  For tiny inputs. */
 int ggrn_oracle_forward_f64(const void* y, const void* gate, const void* w, void* out,

@@ -7,7 +7,7 @@ import torch
 
 import ggrn_inputs
 import oracle
-from tests.tolerance import check, weight_cols
+from tests.tolerance import assert_parity, check, merge, weight_cols
 
 MAMBA2, ONNX = 0, 1
 
@@ -39,17 +39,42 @@ def to_host(inp: ggrn_inputs.Inputs, rows=None) -> ggrn_inputs.Inputs:
 
 
 def oracle_ref(inp_host: ggrn_inputs.Inputs, group_size: int, eps: float, mode: int):
-    """(out, t) from the oracle; t is None in ONNX mode."""
-    if mode == MAMBA2:
-        return oracle.forward(inp_host.y, inp_host.gate, inp_host.w, group_size=group_size,
-                              eps=eps, mode=mode, want_t=True)
-    return oracle.forward(inp_host.y, inp_host.gate, inp_host.w, group_size=group_size, eps=eps,
-                          mode=mode), None
+    """(out, t, pre) from the oracle; t is None in ONNX mode."""
+    return oracle.default().forward_detail(inp_host.y, inp_host.gate, inp_host.w,
+                                           group_size=group_size, eps=eps, mode=mode)
 
 
 def compare(got: torch.Tensor, inp_host: ggrn_inputs.Inputs, group_size: int, eps: float,
-            mode: int) -> dict:
-    ref, t = oracle_ref(inp_host, group_size, eps, mode)
+            mode: int, strict: bool = True) -> dict:
+    """Compare ``got`` with the oracle on ``inp_host``; with ``strict`` (the
+    default) assert the parity rules of tests/tolerance.py (``assert_parity``)."""
+    ref, t, pre = oracle_ref(inp_host, group_size, eps, mode)
     rows, width = ref.shape
     w_cols = weight_cols(inp_host.w, rows, width) if mode == MAMBA2 else None
-    return check(got.cpu().reshape(rows, width), ref, mode=mode, ref_t=t, w_cols=w_cols)
+    res = check(got.cpu().reshape(rows, width), ref, mode=mode, ref_t=t, w_cols=w_cols, pre=pre,
+                gate=inp_host.gate, group_size=group_size)
+    if strict:
+        assert_parity(res)
+    return res
+
+
+def compare_all_rows(got: torch.Tensor, inp_host: ggrn_inputs.Inputs, group_size: int,
+                     eps: float, mode: int, block_rows: int = 2048, workers: int = 0) -> dict:
+    """Every row of ``got`` (host tensor) against the oracle, in blocks of
+    rows spread over the host's cores (the oracle's C call releases the
+    interpreter lock); returns the merged summary (not asserted)."""
+    import concurrent.futures
+    import os
+    rows = got.shape[0]
+    if workers <= 0:
+        workers = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 8
+    starts = list(range(0, rows, block_rows))
+
+    def one(r0):
+        sl = slice(r0, min(rows, r0 + block_rows))
+        blk = ggrn_inputs.Inputs(y=inp_host.y[sl], gate=inp_host.gate[sl], w=inp_host.w)
+        return compare(got[sl], blk, group_size, eps, mode, strict=False)
+
+    with concurrent.futures.ThreadPoolExecutor(max(1, min(workers, len(starts)))) as ex:
+        results = list(ex.map(one, starts))
+    return merge(results)

@@ -22,7 +22,7 @@ MUTANTS = {
     # Mamba-2 weight indexed by j instead of col
     "weight_by_j": ("static_cast<const float*>(w)[col] * t;", "static_cast<const float*>(w)[j] * t;"),
     # no intermediate cast to T before the weight multiply
-    "no_intermediate_cast": ("float t = round_to_t(gated[j] * nf, dtype);", "float t = gated[j] * nf;"),
+    "no_intermediate_cast": ("float t = round_to_t(pre, dtype);", "float t = pre;"),
     # ONNX gated before the norm (Mamba-2 ordering) -- the gate enters m2
     "onnx_gate_first": ("          x[j] = load_elem(y, n * y_row_stride + col0 + j, dtype);\n",
                         "          x[j] = load_elem(y, n * y_row_stride + col0 + j, dtype) *"

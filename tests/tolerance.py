@@ -5,13 +5,53 @@ Floating-point bar (set by the workload statement of this library): every
 result, cast-boundary flips from a different summation order allowed; f32
 outputs within 1e-5 relative.
 
-The Mamba-2 semantics cast twice (t = cast_T(gated*nf), then
-out = cast_T(w*t)).  A different summation order moves m2 by an f32 ulp or so;
-when gated*nf then sits next to a T rounding midpoint, t flips by one T ulp,
-and the second rounding can turn that into 2 ulps of out.  The flip-aware rule
-accepts an element when it is within 1 ulp of the oracle's out, OR within 1
-ulp of cast_T(w * t') with t' a T-neighbour of the oracle's t.  The ONNX
-semantics round once, so 1 ulp is the whole rule there.
+What a correct GPU result can differ in.  The GPU sums the squares of a group
+in another order than the oracle's sequential sum, and computes silu and the
+reciprocal square root with the hardware's approximate instructions, so its
+value of each element just before a rounding to T (``pre``: gated*nf for the
+Mamba-2 intermediate cast, the full product for the ONNX store) differs from
+the oracle's by a small relative amount.  Every other step is the same IEEE
+operation on both sides (the f32 product w*t of the Mamba-2 epilogue, the
+round-to-nearest-even casts).  So an output element can differ from the
+oracle's only through a *flip*: ``pre`` lies so close to a rounding midpoint
+of T that the two sides round it to neighbouring T values.
+
+  * Mamba-2 ("gated_group_rmsnorm" page, math block): t = cast_T(gated*nf)
+    flips to its neighbour t' on the side of the nearer midpoint, and then
+    out = cast_T(w*t') exactly (one f32 multiply, one rounding), which can be
+    2 ulps from the oracle's out.
+  * ONNX ("com.microsoft.GatedRMSNorm" README, Description): one rounding, so
+    the flipped output is the oracle's out's neighbour on that side.
+
+A flip is *explained* when the element equals that flipped value bit for bit
+AND the oracle's ``pre`` lies within ``tau * |pre|`` of the midpoint, where
+tau bounds the relative difference of the two sides' ``pre``.  With u = 2^-24
+(half an f32 ulp, relative), n the group size and b the gate values:
+
+  Mamba-2  tau_j = (n + |b_j| + max_k |b_k| + 48) u   (k over the group)
+  ONNX     tau_j = (n + |b_j| + 48) u
+
+from: any two orders of a sum of n non-negative terms differ by at most
+2(n-1)u relative, halved by the square root; silu's base-2 exponential takes
+an argument rounded by u relative, an absolute error of |b|u in the exponent
+(|b| counted up to 89, beyond which both sides saturate exactly), plus a few
+u for the approximate exponential and reciprocal; a few u for the divide, the
+eps add, the approximate rsqrt (budgeted 8u) and the products.
+
+Rules applied (``check``):
+  ``ok``           the stated bar: each element within 1 ulp of the oracle's,
+                   or an explained Mamba-2 flip (which may be 2 ulps away);
+  ``unexplained``  elements that differ from the oracle's and are not an
+                   explained flip -- zero for a correct kernel, asserted by
+                   ``assert_parity``;
+  ``over1``        elements more than 1 ulp away (all of them explained
+                   flips), bounded by ``MAX_OVER1_RATE``; ``flips`` by
+                   ``MAX_FLIP_RATE``.
+
+The rates: a CPU model of the oracle's sequential sum against a 32-lane tree
+sum on the four prefill workloads flipped 1e-5 to 1.2e-4 of the elements and
+put 0 to 1.6e-5 of them more than 1 ulp away (the 5120-wide groups with
+weights up to 1.5 the most); the bounds sit about eight times above.
 """
 from __future__ import annotations
 
@@ -19,6 +59,11 @@ import torch
 
 F32_RTOL = 1e-5
 F32_ATOL = 1e-30
+U = 2.0 ** -24
+TAU_CONST = 48.0
+SILU_ARG_CAP = 89.0
+MAX_FLIP_RATE = 1e-3
+MAX_OVER1_RATE = 1.3e-4
 
 
 def ordinal(t: torch.Tensor) -> torch.Tensor:
@@ -62,17 +107,53 @@ def neighbours(t: torch.Tensor):
     return from_ordinal(o + 1, t.dtype), from_ordinal(o - 1, t.dtype)
 
 
-def mamba2_accept(got: torch.Tensor, ref: torch.Tensor, ref_t: torch.Tensor,
-                  w_cols: torch.Tensor) -> torch.Tensor:
-    """Per-element acceptance (bool tensor) for 16-bit T under Mamba-2 semantics.
+def flip_target(t: torch.Tensor, pre: torch.Tensor, tau: torch.Tensor):
+    """For each element: the T neighbour t' of ``t`` on the side of ``pre``
+    (the value the other side's rounding gives if it flips), and whether
+    ``pre`` lies within ``tau * |pre|`` of the midpoint between t and t'."""
+    p = pre.double()
+    tv = t.double()
+    up, down = neighbours(t)
+    toward_up = p >= tv
+    tn = torch.where(toward_up, up, down)
+    tnv = tn.double()
+    # a neighbour past the largest finite value: the midpoint is half a
+    # spacing beyond t, the spacing of t's own binade
+    other = torch.where(toward_up, down, up).double()
+    spacing = torch.where(torch.isfinite(tnv), (tnv - tv).abs(), (tv - other).abs())
+    mid = tv + torch.where(toward_up, 0.5, -0.5) * spacing
+    near = (p - mid).abs() <= tau * p.abs()
+    near &= torch.isfinite(p) & torch.isfinite(tv)
+    return tn, near
 
-    ``w_cols``: f32 weight broadcast to ``ref``'s shape (w[col] per element).
-    """
-    ok = ulp_dist(got, ref) <= 1
-    for tn in neighbours(ref_t):
-        alt = (w_cols.float() * tn.float()).to(ref.dtype)
-        ok |= ulp_dist(got, alt) <= 1
-    return ok
+
+def flip_tau(gate: torch.Tensor, group_size: int, mode: int) -> torch.Tensor:
+    """tau per element (see the module docstring), f64, shaped like ``gate``."""
+    b = gate.double().abs().clamp(max=SILU_ARG_CAP)
+    b = torch.where(torch.isnan(b), torch.full_like(b, SILU_ARG_CAP), b)
+    rows, width = b.shape
+    tau = (group_size + TAU_CONST) + b
+    if mode == 0:
+        bmax = b.reshape(rows, width // group_size, group_size).amax(-1, keepdim=True)
+        tau = tau + bmax.expand(rows, width // group_size, group_size).reshape(rows, width)
+    return tau * U
+
+
+def mamba2_accept(got: torch.Tensor, ref: torch.Tensor, ref_t: torch.Tensor,
+                  w_cols: torch.Tensor, pre: torch.Tensor, tau: torch.Tensor):
+    """Per-element (accepted, explained flip) for 16-bit T under Mamba-2
+    semantics.  ``w_cols``: f32 weight broadcast to ``ref``'s shape."""
+    tn, near = flip_target(ref_t, pre, tau)
+    alt = (w_cols.float() * tn.float()).to(ref.dtype)
+    flip = near & (ulp_dist(got, alt) == 0)
+    return (ulp_dist(got, ref) <= 1) | flip, flip
+
+
+def onnx_flip(got: torch.Tensor, ref: torch.Tensor, pre: torch.Tensor,
+              tau: torch.Tensor) -> torch.Tensor:
+    """Explained flips of the single ONNX rounding."""
+    tn, near = flip_target(ref, pre, tau)
+    return near & (ulp_dist(got, tn) == 0)
 
 
 def f32_accept(got: torch.Tensor, ref: torch.Tensor, rtol: float = F32_RTOL,
@@ -85,30 +166,60 @@ def f32_accept(got: torch.Tensor, ref: torch.Tensor, rtol: float = F32_RTOL,
 
 
 def check(got: torch.Tensor, ref: torch.Tensor, *, mode: int, ref_t: torch.Tensor | None = None,
-          w_cols: torch.Tensor | None = None) -> dict:
-    """Apply the rule for ``mode`` (0 Mamba-2, 1 ONNX); return a summary dict.
+          w_cols: torch.Tensor | None = None, pre: torch.Tensor | None = None,
+          gate: torch.Tensor | None = None, group_size: int | None = None) -> dict:
+    """Apply the rules for ``mode`` (0 Mamba-2, 1 ONNX); return a summary dict
+    with ``ok``, ``bad`` (rejected by the stated bar), ``unexplained``,
+    ``flips``, ``over1``, ``max_ulp``, ``same`` (bit-equal by value) and ``n``.
 
-    The summary has ``ok`` (all accepted), ``bad`` (rejected count),
-    ``over1`` (raw count of elements more than 1 ulp from the oracle's out),
-    ``max_ulp`` and ``n``.
+    16-bit T needs the oracle's ``pre`` and the ``gate`` values (for tau) and
+    ``group_size``; Mamba-2 also ``ref_t`` and ``w_cols``.
     """
     got = got.cpu()
     ref = ref.cpu()
+    n = ref.numel()
     if ref.dtype == torch.float32:
         acc = f32_accept(got, ref)
-        over1 = int((~acc).sum())
-        max_ulp = int(ulp_dist(got, ref).max()) if ref.numel() else 0
-    else:
+        bad = int((~acc).sum())
         d = ulp_dist(got, ref)
-        over1 = int((d > 1).sum())
-        max_ulp = int(d.max()) if ref.numel() else 0
-        if mode == 0:
-            assert ref_t is not None and w_cols is not None
-            acc = mamba2_accept(got, ref, ref_t.cpu(), w_cols.cpu())
-        else:
-            acc = d <= 1
+        return {"ok": bad == 0, "bad": bad, "unexplained": bad, "flips": 0, "over1": bad,
+                "max_ulp": int(d.max()) if n else 0, "same": int((d == 0).sum()), "n": n}
+    assert pre is not None and gate is not None and group_size is not None
+    d = ulp_dist(got, ref)
+    tau = flip_tau(gate.cpu(), group_size, mode)
+    if mode == 0:
+        assert ref_t is not None and w_cols is not None
+        acc, flip = mamba2_accept(got, ref, ref_t.cpu(), w_cols.cpu(), pre.cpu(), tau)
+    else:
+        flip = onnx_flip(got, ref, pre.cpu(), tau)
+        acc = d <= 1
+    differ = d != 0
     bad = int((~acc).sum())
-    return {"ok": bad == 0, "bad": bad, "over1": over1, "max_ulp": max_ulp, "n": ref.numel()}
+    return {"ok": bad == 0, "bad": bad,
+            "unexplained": int((differ & ~flip).sum()),
+            "flips": int((differ & flip).sum()),
+            "over1": int((d > 1).sum()),
+            "max_ulp": int(d.max()) if n else 0,
+            "same": int((~differ).sum()), "n": n}
+
+
+def merge(results: list[dict]) -> dict:
+    """Sum the counts of several ``check`` summaries (blocks of one output)."""
+    out = {"ok": all(r["ok"] for r in results)}
+    for k in ("bad", "unexplained", "flips", "over1", "same", "n"):
+        out[k] = sum(r[k] for r in results)
+    out["max_ulp"] = max((r["max_ulp"] for r in results), default=0)
+    return out
+
+
+def assert_parity(res: dict, what="") -> None:
+    """The stated bar, no unexplained difference, and the rate bounds."""
+    assert res["ok"], (what, res)
+    assert res["unexplained"] == 0, (what, res)
+    n = max(res["n"], 1)
+    # a floor of a few elements keeps tiny cases from tripping on one flip
+    assert res["flips"] <= MAX_FLIP_RATE * n + 4, (what, res)
+    assert res["over1"] <= MAX_OVER1_RATE * n + 2, (what, res)
 
 
 def weight_cols(w: torch.Tensor, rows: int, width: int) -> torch.Tensor:
