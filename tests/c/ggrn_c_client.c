@@ -12,6 +12,13 @@
  *       ggrn_forward_host on pinned host copies, checks the device status
  *       word, and writes the ggrn_forward output to OUT and the
  *       ggrn_forward_host output to OUT.host.
+ *   ggrn_c_client packed IN OUT ROWS WIDTH GS DTYPE MODE EPS PACKED_WIDTH GATE_COL
+ *       IN holds one packed matrix (ROWS x PACKED_WIDTH elements of T; y is
+ *       its columns [0, WIDTH), gate its columns [GATE_COL, GATE_COL +
+ *       WIDTH)) and the weight.  Runs ggrn_forward on the two strided views
+ *       (row stride PACKED_WIDTH), ggrn_forward_inproj on the packed matrix
+ *       and ggrn_forward_host on a pinned host copy of it; writes OUT,
+ *       OUT.inproj and OUT.host (contiguous ROWS x WIDTH outputs).
  *
  * The client only moves bytes: inputs come from the tests' seeded generator
  * and the outputs are checked against the oracle by the tests.
@@ -138,9 +145,100 @@ static int run(int argc, char** argv) {
   return 0;
 }
 
+static int write_file(const char* path, const char* suffix, const void* data, size_t n) {
+  char name[4096];
+  snprintf(name, sizeof(name), "%s%s", path, suffix);
+  FILE* f = fopen(name, "wb");
+  if (!f) return 2;
+  const size_t w = fwrite(data, 1, n, f);
+  fclose(f);
+  return w == n ? 0 : 2;
+}
+
+static int packed(int argc, char** argv) {
+  if (argc != 12) {
+    fprintf(stderr, "usage: packed IN OUT ROWS WIDTH GS DTYPE MODE EPS PACKED_WIDTH GATE_COL\n");
+    return 1;
+  }
+  const char* in_path = argv[2];
+  const char* out_path = argv[3];
+  const int64_t rows = atoll(argv[4]), width = atoll(argv[5]), gs = atoll(argv[6]);
+  const int dtype = atoi(argv[7]), mode = atoi(argv[8]);
+  const float eps = (float)atof(argv[9]);
+  const int64_t pw = atoll(argv[10]), gcol = atoll(argv[11]);
+  const size_t es = dtype == GGRN_F32 ? 4 : 2;
+  const size_t pbytes = (size_t)rows * (size_t)pw * es;
+  const size_t obytes = (size_t)rows * (size_t)width * es;
+  const size_t wbytes = mode == GGRN_MODE_MAMBA2 ? (size_t)width * 4 : (size_t)gs * es;
+
+  unsigned char *hp, *hw, *ho, *ho_host;
+  CUDA_OK(cudaMallocHost((void**)&hp, pbytes));
+  CUDA_OK(cudaMallocHost((void**)&ho_host, obytes));
+  hw = (unsigned char*)malloc(wbytes);
+  ho = (unsigned char*)malloc(obytes);
+  if (!hw || !ho) return 2;
+  FILE* f = fopen(in_path, "rb");
+  if (!f) return 2;
+  if (fread(hp, 1, pbytes, f) != pbytes || fread(hw, 1, wbytes, f) != wbytes) {
+    fprintf(stderr, "short input file\n");
+    return 2;
+  }
+  fclose(f);
+
+  void *dp, *dw, *dout;
+  CUDA_OK(cudaMalloc(&dp, pbytes));
+  CUDA_OK(cudaMalloc(&dw, wbytes));
+  CUDA_OK(cudaMalloc(&dout, obytes));
+  CUDA_OK(cudaMemcpy(dp, hp, pbytes, cudaMemcpyHostToDevice));
+  CUDA_OK(cudaMemcpy(dw, hw, wbytes, cudaMemcpyHostToDevice));
+  const unsigned char* dy = (const unsigned char*)dp;
+  const unsigned char* dg = dy + (size_t)gcol * es;
+
+  uint32_t flags = 0;
+  ggrn_fault_status(&flags, 1);
+  int rc = 0;
+  CUDA_OK(cudaMemset(dout, 0, obytes));
+  int st = ggrn_forward(dy, dg, dw, dout, rows, width, gs, pw, pw, width, eps, dtype, mode, NULL);
+  printf("forward %d\n", st);
+  if (st != GGRN_OK) return 3;
+  CUDA_OK(cudaDeviceSynchronize());
+  CUDA_OK(cudaMemcpy(ho, dout, obytes, cudaMemcpyDeviceToHost));
+  rc |= write_file(out_path, "", ho, obytes);
+
+  CUDA_OK(cudaMemset(dout, 0, obytes));
+  st = ggrn_forward_inproj(dp, pw, 0, gcol, dw, dout, width, rows, width, gs, eps, dtype, mode,
+                           NULL);
+  printf("forward_inproj %d\n", st);
+  if (st != GGRN_OK) return 3;
+  CUDA_OK(cudaDeviceSynchronize());
+  CUDA_OK(cudaMemcpy(ho, dout, obytes, cudaMemcpyDeviceToHost));
+  rc |= write_file(out_path, ".inproj", ho, obytes);
+
+  memset(ho_host, 0, obytes);
+  st = ggrn_forward_host(hp, hp + (size_t)gcol * es, dw, ho_host, rows, width, gs, pw, pw, width,
+                         eps, dtype, mode, NULL, 0, NULL);
+  printf("forward_host %d\n", st);
+  if (st != GGRN_OK) return 3;
+  CUDA_OK(cudaDeviceSynchronize());
+  rc |= write_file(out_path, ".host", ho_host, obytes);
+  ggrn_fault_status(&flags, 0);
+  printf("fault %u\n", flags);
+
+  cudaFree(dp);
+  cudaFree(dw);
+  cudaFree(dout);
+  cudaFreeHost(hp);
+  cudaFreeHost(ho_host);
+  free(hw);
+  free(ho);
+  return rc;
+}
+
 int main(int argc, char** argv) {
   if (argc >= 2 && strcmp(argv[1], "validate") == 0) return validate();
   if (argc >= 2 && strcmp(argv[1], "run") == 0) return run(argc, argv);
-  fprintf(stderr, "usage: %s validate | run IN OUT ROWS WIDTH GS DTYPE MODE EPS\n", argv[0]);
+  if (argc >= 2 && strcmp(argv[1], "packed") == 0) return packed(argc, argv);
+  fprintf(stderr, "usage: %s validate | run IN OUT ROWS WIDTH GS DTYPE MODE EPS | packed ...\n",
+          argv[0]);
   return 1;
 }

@@ -59,22 +59,41 @@ def compare(got: torch.Tensor, inp_host: ggrn_inputs.Inputs, group_size: int, ep
 
 
 def compare_all_rows(got: torch.Tensor, inp_host: ggrn_inputs.Inputs, group_size: int,
-                     eps: float, mode: int, block_rows: int = 2048, workers: int = 0) -> dict:
-    """Every row of ``got`` (host tensor) against the oracle, in blocks of
-    rows spread over the host's cores (the oracle's C call releases the
-    interpreter lock); returns the merged summary (not asserted)."""
+                     eps: float, mode: int, block_rows: int = 1024, workers: int = 0) -> dict:
+    """Every row of ``got`` (host tensor) against the oracle; returns the
+    summary (not asserted).  The oracle runs over blocks of rows on all host
+    cores (its C call releases the interpreter lock), then the rules are
+    applied to larger blocks with torch's own threads."""
     import concurrent.futures
     import os
-    rows = got.shape[0]
+    rows, width = got.shape
     if workers <= 0:
         workers = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 8
-    starts = list(range(0, rows, block_rows))
+    dtype = inp_host.y.dtype
+    ref = torch.empty((rows, width), dtype=dtype)
+    t = torch.empty((rows, width), dtype=dtype) if mode == MAMBA2 else None
+    pre = torch.empty((rows, width), dtype=torch.float32)
+    orc = oracle.default()
 
     def one(r0):
         sl = slice(r0, min(rows, r0 + block_rows))
-        blk = ggrn_inputs.Inputs(y=inp_host.y[sl], gate=inp_host.gate[sl], w=inp_host.w)
-        return compare(got[sl], blk, group_size, eps, mode, strict=False)
+        o, tt, pp = orc.forward_detail(inp_host.y[sl], inp_host.gate[sl], inp_host.w,
+                                       group_size=group_size, eps=eps, mode=mode)
+        ref[sl] = o
+        pre[sl] = pp
+        if t is not None:
+            t[sl] = tt
 
+    starts = list(range(0, rows, block_rows))
     with concurrent.futures.ThreadPoolExecutor(max(1, min(workers, len(starts)))) as ex:
-        results = list(ex.map(one, starts))
+        list(ex.map(one, starts))
+    results = []
+    step = max(1, (1 << 24) // width)  # about 16 M elements per check
+    for r0 in range(0, rows, step):
+        sl = slice(r0, min(rows, r0 + step))
+        n = sl.stop - sl.start
+        w_cols = weight_cols(inp_host.w, n, width) if mode == MAMBA2 else None
+        results.append(check(got[sl], ref[sl], mode=mode, ref_t=t[sl] if t is not None else None,
+                             w_cols=w_cols, pre=pre[sl], gate=inp_host.gate[sl],
+                             group_size=group_size))
     return merge(results)

@@ -190,7 +190,7 @@ def test_binding_rejects_cpu_tensors():
 def test_noalloc_rejects_before_touching_the_device():
     """The allocation-free entry point validates and plans on the host: bad
     arguments, shapes its kernel family cannot stream, and calls beyond its
-    counter's limit return before any CUDA call."""
+    counter's limit return before any allocation or launch."""
     def call(**kw):
         args = dict(y=Y, gate=GATE, w=W, out=OUT, rows=4, width=64, gs=32, ys=64, gts=64, os_=64,
                     dtype=2, mode=0)
@@ -209,6 +209,39 @@ def test_noalloc_rejects_before_touching_the_device():
     # limit, 2^31 is beyond it (fake, far-apart addresses; nothing is read)
     big = dict(y=1 << 46, gate=2 << 46, w=3 << 46, out=4 << 46, width=32, ys=32, gts=32, os_=32)
     assert call(rows=1 << 39, **big) == binding.ERR_LIMIT
+
+
+def _stream_units(rows, width, gs, dtype=2, mode=0):
+    st, info = g.ggrn_plan(1 << 46, 2 << 46, 3 << 46, 4 << 46, rows, width, gs, width, width,
+                           width, dtype, mode, g.PATH_STREAM)
+    assert st == binding.OK
+    return info.items
+
+
+def test_noalloc_limit_boundary():
+    """A call of exactly GGRN_NOALLOC_MAX_UNITS streamed units passes the
+    limit check, one more unit does not.  Without a device the call that
+    passes then stops at its first CUDA call (the scratch address lookup);
+    with one it would launch on the fake addresses, so it is not run there."""
+    if torch.cuda.is_available():
+        pytest.skip("would launch a kernel on fake addresses")
+    limit = 1 << 30
+    width = gs = 32
+    lo, hi = 1, 1 << 40          # rows with at most / more than `limit` units
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if _stream_units(mid, width, gs) <= limit:
+            lo = mid
+        else:
+            hi = mid
+    assert _stream_units(lo, width, gs) == limit, "no row count gives exactly the limit"
+    assert _stream_units(hi, width, gs) == limit + 1
+
+    def call(rows):
+        return g.ggrn_forward_noalloc(1 << 46, 2 << 46, 3 << 46, 4 << 46, rows, width, gs, width,
+                                      width, width, 1e-5, 2, 0, None)
+    assert call(hi) == binding.ERR_LIMIT
+    assert call(lo) == binding.ERR_CUDA     # past the check: no device to look the scratch up on
 
 
 def test_inproj_validation():

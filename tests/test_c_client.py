@@ -15,6 +15,7 @@ import ggrn_inputs
 import gated_group_rmsnorm_gb300 as g
 from gated_group_rmsnorm_gb300 import binding, build
 from tests import gpu_util
+from tests.tolerance import assert_parity
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "tests", "c", "ggrn_c_client.c")
@@ -92,3 +93,33 @@ def test_c_client_matches_oracle(client, tmp_path, name, rows):
         out = raw.view(wl.dtype).reshape(rows, wl.width)
         res = gpu_util.compare(out, host, wl.group_size, wl.eps, wl.mode)
         assert res["ok"], (path.name, res)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rows", [1531, 65536])
+def test_c_client_strided_views(client, tmp_path, rows):
+    """The strided workload's packed in-proj layout from C: the two strided
+    views through ggrn_forward, the packed matrix through
+    ggrn_forward_inproj, and pinned host memory (read in place) through
+    ggrn_forward_host, every row against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wl = ggrn_inputs.WORKLOADS["strided_odd_span"].with_rows(rows)
+    host = ggrn_inputs.make_inputs(wl, seed=rows)
+    src, dst = tmp_path / "in.bin", tmp_path / "out.bin"
+    src.write_bytes(_bytes(host.packed) + _bytes(host.w))
+    r = subprocess.run([client, "packed", str(src), str(dst), str(rows), str(wl.width),
+                        str(wl.group_size), str(binding.DTYPE_CODE[wl.dtype]), str(wl.mode),
+                        repr(wl.eps), str(wl.packed_width), str(wl.width)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, (r.stdout, r.stderr)
+    got = _lines(r.stdout)
+    for k in ("forward", "forward_inproj", "forward_host"):
+        assert int(got[k]) == binding.OK, (k, got)
+    assert got["fault"] == "0"
+    for suffix in ("", ".inproj", ".host"):
+        raw = torch.frombuffer(bytearray((tmp_path / ("out.bin" + suffix)).read_bytes()),
+                               dtype=torch.int16)
+        out = raw.view(wl.dtype).reshape(rows, wl.width)
+        res = gpu_util.compare_all_rows(out, host, wl.group_size, wl.eps, wl.mode)
+        assert_parity(res, "c client " + (suffix or "forward"))

@@ -7,6 +7,7 @@ import torch
 import ggrn_inputs
 import gated_group_rmsnorm_gb300 as g
 from tests import gpu_util
+from tests.tolerance import assert_parity
 
 pytestmark = pytest.mark.gpu
 MAMBA2, ONNX = 0, 1
@@ -83,16 +84,17 @@ def test_leading_axes_and_strided_out():
     assert bool((big[..., :32] == -1280.0).all()) and bool((big[..., 4832:] == -1280.0).all())
 
 
-def test_full_size_strided_workload_sampled():
+def test_full_size_strided_workload_all_rows():
     """The strided workload's full packed buffer through the in-proj entry
-    point: sampled rows against the oracle."""
+    point: every row against the oracle, and the same bits as the view path."""
     wl = ggrn_inputs.WORKLOADS["strided_odd_span"]
     dev = ggrn_inputs.make_inputs(wl, device="cuda")
     out = g.forward_inproj(dev.packed, dev.w, width=wl.width, y_col=0, gate_col=wl.width,
                            group_size=wl.group_size, eps=wl.eps)
+    ref = g.forward(dev.y, dev.gate, dev.w, group_size=wl.group_size, eps=wl.eps)
     torch.cuda.synchronize()
-    rows = [0, 1, 12345, 40000, wl.rows - 1]
-    host = gpu_util.to_host(dev, rows)
-    got = out.index_select(0, torch.tensor(rows, device=out.device)).cpu()
-    res = gpu_util.compare(got, host, wl.group_size, wl.eps, wl.mode)
-    assert res["ok"], res
+    assert torch.equal(_bits(out), _bits(ref))
+    host = gpu_util.to_host(dev)
+    res = gpu_util.compare_all_rows(out.cpu(), host, wl.group_size, wl.eps, wl.mode)
+    print("strided_odd_span via forward_inproj, all rows:", res)
+    assert_parity(res, "strided_odd_span inproj")

@@ -11,7 +11,7 @@ import torch
 import ggrn_inputs
 import gated_group_rmsnorm_gb300 as g
 from tests import gpu_util
-from tests.tolerance import ulp_dist
+from tests.tolerance import assert_parity, parity_ok, ulp_dist
 
 pytestmark = pytest.mark.gpu
 
@@ -51,8 +51,10 @@ def test_workload_small(name):
 
 
 @pytest.mark.parametrize("name", sorted(WL))
-def test_workload_full_size_sampled(name):
-    """Full size, the launch the benchmark times; the oracle checks sampled rows."""
+def test_workload_full_size_all_rows(name):
+    """Full size, the launch the benchmark times: every row against the oracle
+    (the streaming kernels' claimed schedule decides which CTA writes which
+    rows), and two calls give the same bits."""
     wl = WL[name]
     dev = ggrn_inputs.make_inputs(wl, device="cuda")
     out = _run(dev, wl)
@@ -61,14 +63,12 @@ def test_workload_full_size_sampled(name):
     assert torch.equal(out.view(torch.int16) if out.dtype != torch.float32 else out,
                        out2.view(torch.int16) if out2.dtype != torch.float32 else out2), \
         "two calls on the same input differ"
-    gen = torch.Generator().manual_seed(99)
-    n = wl.rows
-    rows = sorted(set([0, n - 1, n // 2] + torch.randint(0, n, (29,), generator=gen).tolist()))
-    host = gpu_util.to_host(dev, rows)
-    got = out.index_select(0, torch.tensor(rows, device=out.device)).cpu()
-    res = gpu_util.compare(got, host, wl.group_size, wl.eps, wl.mode)
-    assert res["ok"], res
-    assert not torch.isnan(out.float()).any()
+    host = gpu_util.to_host(dev)
+    got = out.cpu()
+    del out2
+    res = gpu_util.compare_all_rows(got, host, wl.group_size, wl.eps, wl.mode)
+    print(f"{name} all {wl.rows} rows:", res)
+    assert_parity(res, name)
 
 
 # group sizes: below, at and above the vector width, the warp width, the
@@ -111,8 +111,8 @@ def test_sweep_every_path(dtype, mode):
                     continue
                 torch.cuda.synchronize()
                 covered[path] += 1
-                res = gpu_util.compare(out, inp, gs, 1e-5, mode)
-                if not res["ok"]:
+                res = gpu_util.compare(out, inp, gs, 1e-5, mode, strict=False)
+                if not parity_ok(res):
                     failures.append((gs, rows, ngroups, g.PATH_NAMES[path], res))
     assert not failures, failures[:10]
     for p in PATHS:

@@ -4,9 +4,10 @@ loop must not block in the driver's allocator, or all device memory comes
 from a pool the caller does not control).
 
 It runs the streaming kernel with its unit-claim counter in a fixed array
-inside the library.  Two calls in a row through the C ABI must each give the
-output of the library's main entry point, ggrn_forward: the second call finds
-the first call's counter in the shared array and must clear it.
+inside the library.  Two calls in a row through the C ABI must each agree
+with the oracle under the parity rules of every other entry point, and give
+the output of the library's main entry point, ggrn_forward: the second call
+finds the first call's counter in the shared array and must clear it.
 
 The file is named to be collected last, so that a run stopping at the first
 failure has run every other test before this one.
@@ -55,8 +56,11 @@ def test_two_calls_match_the_main_entry_point(name, rows):
     for o in outs:
         assert _noalloc(dev, wl, o) == binding.OK
     torch.cuda.synchronize()
+    host = gpu_util.to_host(dev)
     for o in outs:
-        # the tolerance of the parity tests (1 ulp of T); the same kernel
-        # family as the main entry point here, so in practice the same bits
+        # the oracle, under the parity rules of the other entry points
+        gpu_util.compare(o, host, wl.group_size, wl.eps, wl.mode)
+        # and the main entry point, within the same 1 ulp of T (the same
+        # kernel family here, so in practice the same bits)
         assert int(ulp_dist(o.cpu(), ref.cpu()).max()) <= 1
     assert g.fault_status() == 0
