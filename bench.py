@@ -3,17 +3,23 @@
 Prints ONE JSON line (rank 0).  A step is one call of the whole operation
 (validate, select, one kernel: load y/gate, gate, group reduction,
 normaliser, epilogue, store) over one batch of synthetic input.  Default
-workload: the Mamba-2 prefill shape (4096 rows x 7680, groups of 960, bf16).
+workload: the largest prefill shape that one GPU holds, the strided odd span
+(65536 rows x 4800, groups of 100, bf16, y and gate column slices of a packed
+[65536, 9664] in-proj output).
 
-  value      algorithmic HBM GB/s (y + gate read once, out written once, the
-             weight once) / device time of the K timed steps, summed over ranks
-  e2e        the same metric through the public Python API with pinned HOST
-             buffers: host->device copy of y and gate, the call, device->host
-             copy of out, every step
-  roofline   the kernel's achieved GB/s against the measured HBM copy peak;
-             traffic = DRAM bytes per launch from the ncu capture recorded in
-             profiles/dram_traffic.txt (null when the kernels changed since)
-  cpu_baseline  the single-threaded CPU oracle on a bounded sample
+  value        algorithmic HBM GB/s (y + gate read once, out written once, the
+               weight once) / device time of the K timed steps, summed over ranks
+  per_config   the other prefill workloads, each timed the same way in its own
+               window (max(K, 50) steps), with its roofline and clocks
+  e2e          the same metric through the public Python API with pinned HOST
+               buffers, every byte crossing the host link inside the timed region
+  roofline     the kernel's achieved GB/s against the measured HBM copy peak;
+               traffic = DRAM bytes per launch from the ncu range capture
+               recorded in profiles/dram_traffic.txt (null when the kernels
+               changed since)
+  clocks       SM clock, power and clock-event reasons sampled in process
+               (NVML, read-only) during each timed region
+  cpu_baseline the single-threaded CPU oracle on a bounded sample
 
 Timing: W warm-up steps, then K steps between two CUDA events on the
 launching stream with a barrier and a synchronize on both sides, max over
@@ -92,63 +98,81 @@ def aggregate(bytes_per_step: int, rows_per_step: int, steps: int, max_ms: float
 # Clock sampling during the timed region.
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    """SM clock, power and clock-event reasons sampled in this process through
+    NVML's read-only queries, about every millisecond, so that even a timed
+    region of a fraction of a millisecond has samples around it.  Nothing is
+    ever set: only nvmlDeviceGet* calls are made."""
+    # clock-event reason bits of the NVML header
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
 
-    def __init__(self, uuid: str, period_ms: int = 50):
-        self.uuid = uuid.replace("GPU-", "").lower()
-        self.samples: list[tuple[float, list[str]]] = []
-        self.proc = None
+    def __init__(self, uuid: str, period_s: float = 0.001):
+        self.samples: list[tuple[float, int, int, int]] = []  # (time, sm MHz, reasons, mW)
+        self.max_mhz = None
+        self.error = None
+        self._stop = threading.Event()
+        self.thread = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                text=True)
-        except OSError:
-            self.proc = None
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if L.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) != 0:
+                raise OSError(f"no NVML device with uuid {u}")
+            mx = ctypes.c_uint()
+            if L.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.L, self.h = L, h
+        except (OSError, AttributeError) as e:
+            self.error = str(e)
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.period = period_s
+        self.thread = threading.Thread(target=self._run, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) == 9 and parts[0].replace("GPU-", "").lower() == self.uuid:
-                self.samples.append((time.time(), parts))
+    def _run(self):
+        L, h = self.L, self.h
+        mhz, rs, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self._stop.is_set():
+            ok = L.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) == 0
+            if ok and L.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) != 0:
+                rs.value = 0
+            if L.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) != 0:
+                mw.value = 0
+            if ok:
+                self.samples.append((time.perf_counter(), mhz.value, rs.value, mw.value))
+            time.sleep(self.period)
 
     def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
 
     def summary(self, t0: float, t1: float) -> dict:
-        win = [p for t, p in self.samples if t0 <= t <= t1]
-        window = "timed"
-        if len(win) < 3:  # short timed region: widen to the samples around it
-            win = [p for t, p in self.samples if t0 - 1.0 <= t <= t1 + 0.2]
-            window = "timed+1s before"
-        if not win:
+        """Samples taken while the timed region ran (host clock, perf_counter);
+        for a region shorter than a few sampling periods, the samples of the
+        2 ms either side of it as well."""
+        if self.error is not None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "window": "none (nvidia-smi unavailable)"}
-
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-        sm = [num(p[1]) for p in win if num(p[1]) is not None]
-        mx = [num(p[2]) for p in win if num(p[2]) is not None]
-        pw = [num(p[3]) for p in win if num(p[3]) is not None]
-        reasons = sorted({r for p in win for r, v in zip(self.REASONS, p[5:9]) if v == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(win), "window": window}
+                    "window": f"none (NVML unavailable: {self.error})"}
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if len(win) < 3:
+            win = [s for s in self.samples if t0 - 0.002 <= s[0] <= t1 + 0.002]
+            window = "timed region +-2 ms"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "window": window}
+        reasons = sorted({name for _, _, r, _ in win for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(m for _, m, _, _ in win),
+                "sm_min_mhz": min(m for _, m, _, _ in win),
+                "sm_max_mhz": self.max_mhz,
+                "power_w_max": round(max(p for _, _, _, p in win) / 1000.0, 1),
+                "reasons": reasons, "samples": len(win), "window": window,
+                "source": "NVML queries in the bench process, ~1 ms apart"}
 
 
 # ---------------------------------------------------------------------------
@@ -459,6 +483,72 @@ def _unfused_chain(wl, sets, steps: int) -> dict:
                     "algorithmic bytes and inputs; context for the single fused launch"}
 
 
+def _time_workload(g, L, wl, steps: int, warmup: int, device, sampler) -> dict:
+    """W untimed steps, then exactly K steps of one workload between CUDA events
+    on the launching stream, barrier + synchronize on both sides; inputs
+    rotate over copies whose total exceeds the L2.  Returns the measurement
+    (max over ranks) with the plan and the clock samples of the region."""
+    bytes_per_step = wl.algorithmic_bytes()
+    n_sets = max(2, -(-4 * L2_BYTES // bytes_per_step))
+    sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
+    outs = [torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(device)
+    handle = ctypes.c_void_p(stream.cuda_stream)
+    raw = [_raw_args(g, st, o, wl, handle) for st, o in zip(sets, outs)]
+    plan = g.plan(sets[0].y, sets[0].gate, sets[0].w, group_size=wl.group_size, mode=wl.mode,
+                  out=outs[0])
+    for i in range(warmup):
+        st = L.ggrn_forward(*raw[i % n_sets])
+        if st != 0:
+            raise RuntimeError(f"ggrn_forward: {g.status_string(st)}")
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start = time.perf_counter()
+    e0.record(stream)
+    for i in range(steps):
+        L.ggrn_forward(*raw[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    max_ms = reduce_max(ms, device)
+    res = {"ms": ms, "max_ms": max_ms, "plan": plan, "n_sets": n_sets,
+           "bytes_per_step": bytes_per_step, "clocks": sampler.summary(t_start, t_end),
+           "sets": sets}
+    del outs, raw
+    return res
+
+
+def _roofline(wl, kernel_gbs: float) -> dict:
+    peak, peak_src = hbm_peak()
+    traffic, traffic_note = recorded_traffic(wl.name)
+    return {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(kernel_gbs / peak, 4), "traffic": traffic, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": wl.algorithmic_bytes(),
+            "traffic_note": traffic_note,
+            "ncu_dram_gbs": recorded_ncu_gbs(wl.name),
+            "ncu_dram_gbs_note": "DRAM read+write bytes over the duration of a range of "
+                                 "back-to-back launches under ncu (profiles/dram_traffic.txt)"}
+
+
+def _config(wl, m) -> dict:
+    plan = m["plan"]
+    return {"workload": wl.name, "rows": wl.rows, "width": wl.width,
+            "group_size": wl.group_size, "io_dtype": IO_DTYPE[wl.dtype],
+            "mode": "mamba2" if wl.mode == 0 else "onnx", "eps": wl.eps,
+            "row_stride": wl.packed_width or wl.width,
+            "l2": f"inputs rotate over {m['n_sets']} copies "
+                  f"({m['n_sets'] * m['bytes_per_step'] / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2)",
+            "path": plan["path_name"], "block_threads": plan["block_threads"],
+            "grid_blocks": plan["grid_blocks"]}
+
+
+PER_CONFIG = ("mamba2_prefill", "wide_single_group", "gdn_onnx", "strided_odd_span")
+
+
 def run_ours(args) -> None:
     rank, world, local_rank = dist_env()
     import torch.distributed as dist
@@ -468,49 +558,40 @@ def run_ours(args) -> None:
     device = torch.device("cuda", local_rank)
     import gated_group_rmsnorm_gb300 as g
     L = g.load(build_if_missing=True)
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
 
     wl = ggrn_inputs.WORKLOADS[args.workload]
     if args.rows:
         wl = wl.with_rows(args.rows)
-    bytes_per_step = wl.algorithmic_bytes()
-    n_sets = max(2, -(-4 * L2_BYTES // bytes_per_step))
-    sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
-    outs = [torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device) for _ in range(n_sets)]
-    stream = torch.cuda.current_stream(device)
-    handle = ctypes.c_void_p(stream.cuda_stream)
-    raw = [_raw_args(g, s, o, wl, handle) for s, o in zip(sets, outs)]
-    plan = g.plan(sets[0].y, sets[0].gate, sets[0].w, group_size=wl.group_size, mode=wl.mode,
-                  out=outs[0])
+    m = _time_workload(g, L, wl, args.steps, args.warmup, device, sampler)
+    sets = m.pop("sets")
+    bytes_per_step = m["bytes_per_step"]
+    agg = aggregate(bytes_per_step, wl.rows, args.steps, m["max_ms"], world)
+    kernel_gbs = bytes_per_step / (m["ms"] / args.steps / 1e3) / 1e9
+    peak, _ = hbm_peak()
 
-    props = torch.cuda.get_device_properties(device)
-    sampler = ClockSampler(str(getattr(props, "uuid", "")))
-
-    for i in range(args.warmup):
-        st = L.ggrn_forward(*raw[i % n_sets])
-        if st != 0:
-            raise RuntimeError(f"ggrn_forward: {g.status_string(st)}")
-    torch.cuda.synchronize()
-
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        L.ggrn_forward(*raw[i % n_sets])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_end = time.time()
-    barrier()
-    ms = e0.elapsed_time(e1)
-    max_ms = reduce_max(ms, device)
-    sampler.stop()
-    clocks = sampler.summary(t_start, t_end)
-
-    agg = aggregate(bytes_per_step, wl.rows, args.steps, max_ms, world)
-    peak, peak_src = hbm_peak()
-    kernel_gbs = bytes_per_step / (ms / args.steps / 1e3) / 1e9
-    traffic, traffic_note = recorded_traffic(wl.name)
+    # the other prefill workloads, each timed the same way in its own window
+    per_config = {}
+    if not args.no_per_config and not args.rows:
+        pc_steps, pc_warmup = max(args.steps, 50), max(args.warmup, 5)
+        for name in PER_CONFIG:
+            if name == wl.name:
+                continue
+            pwl = ggrn_inputs.WORKLOADS[name]
+            pm = _time_workload(g, L, pwl, pc_steps, pc_warmup, device, sampler)
+            pm.pop("sets")
+            pagg = aggregate(pm["bytes_per_step"], pwl.rows, pc_steps, pm["max_ms"], world)
+            pgbs = pm["bytes_per_step"] / (pm["ms"] / pc_steps / 1e3) / 1e9
+            per_config[name] = {
+                "value": round(pagg["gbs"], 2), "unit": UNIT, "steps": pc_steps,
+                "warmup": pc_warmup, "ms_per_step": round(pagg["ms_per_step"], 6),
+                "rows_per_s": round(pagg["rows_per_s"], 1),
+                "pct_of_nominal_8TBs": round(100 * pgbs / NOMINAL_HBM_GBS, 2),
+                "launches_per_step": 1, "share_of_timed_region": 1.0,
+                "config": _config(pwl, pm), "roofline": _roofline(pwl, pgbs),
+                "clocks": pm["clocks"]}
+            torch.cuda.empty_cache()
 
     extra = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -518,50 +599,73 @@ def run_ours(args) -> None:
         extra["cpu_baseline_all_cores"] = _cpu_baseline_all_cores(wl, args.cpu_seconds / 2)
     e2e = None
     if not args.no_e2e:
+        t0 = time.perf_counter()
         e2e = _e2e(g, wl, args.e2e_steps, device)
+        e2e["clocks"] = sampler.summary(t0, time.perf_counter())
         e2e_ms = reduce_max(e2e["ms_per_step"], device)
         e2e["value"] = round(world * bytes_per_step / (e2e_ms / 1e3) / 1e9, 2)
         e2e["ms_per_step"] = round(e2e_ms, 4)
     decode = _decode_numbers(g, device) if (rank == 0 and not args.no_decode) else None
     if rank == 0 and world == 1 and not args.no_unfused:
         extra["unfused_chain"] = _unfused_chain(wl, sets, min(args.steps, 200))
+    del sets
+    sampler.stop()
 
     if rank != 0:
         return
+    cfg = _config(wl, m)
+    cfg["parallelism"] = f"replicas x{world} (rows are independent; no collective)"
     line = {
         "metric": METRIC, "value": round(agg["gbs"], 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name, "rows": wl.rows, "width": wl.width,
-                   "group_size": wl.group_size, "io_dtype": IO_DTYPE[wl.dtype],
-                   "mode": "mamba2" if wl.mode == 0 else "onnx", "eps": wl.eps,
-                   "row_stride": wl.packed_width or wl.width,
-                   "l2": f"inputs rotate over {n_sets} copies "
-                         f"({n_sets * bytes_per_step / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2)",
-                   "parallelism": f"replicas x{world} (rows are independent; no collective)",
-                   "path": plan["path_name"], "block_threads": plan["block_threads"],
-                   "grid_blocks": plan["grid_blocks"]},
+        "config": cfg,
         "rows_per_s": round(agg["rows_per_s"], 1),
         "pct_of_peak": {"of_measured_copy_peak": round(100 * kernel_gbs / peak, 2),
                         "of_nominal_8TBs": round(100 * kernel_gbs / NOMINAL_HBM_GBS, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
-                     "traffic": traffic, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": bytes_per_step,
-                     "traffic_note": traffic_note,
-                     "ncu_dram_gbs": recorded_ncu_gbs(wl.name),
-                     "ncu_dram_gbs_note": "DRAM read+write bytes over the duration of one cold "
-                                          "launch under ncu; writes still dirty in L2 at the "
-                                          "kernel's end are not counted"},
-        "clocks": clocks,
+        "roofline": _roofline(wl, kernel_gbs),
+        "clocks": m["clocks"],
         "gpu_launches": args.steps,
         "e2e": e2e,
     }
+    if per_config:
+        line["per_config"] = per_config
     line.update(extra)
     if decode is not None:
         line["decode"] = decode
     print(json.dumps(line), flush=True)
+
+
+def run_profile_range(args) -> None:
+    """For an ncu range capture: W warm-up launches, then N back-to-back
+    launches between cudaProfilerStart and cudaProfilerStop (an ncu range), so
+    DRAM traffic is counted over consecutive launches, including each
+    launch's output written back from L2 during the next one."""
+    import gated_group_rmsnorm_gb300 as g
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    L = g.load(build_if_missing=True)
+    wl = ggrn_inputs.WORKLOADS[args.workload]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
+    n_sets = max(2, -(-4 * L2_BYTES // wl.algorithmic_bytes()))
+    sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
+    outs = [torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(device)
+    raw = [_raw_args(g, st, o, wl, ctypes.c_void_p(stream.cuda_stream))
+           for st, o in zip(sets, outs)]
+    for i in range(args.warmup):
+        assert L.ggrn_forward(*raw[i % n_sets]) == 0
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    for i in range(args.profile_range):
+        L.ggrn_forward(*raw[i % n_sets])
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    print(json.dumps({"workload": wl.name, "rows": wl.rows, "launches_in_range": args.profile_range,
+                      "algorithmic_bytes_per_launch": wl.algorithmic_bytes(),
+                      "csrc_sha": kernel_source_hash()}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -701,7 +805,7 @@ def main(argv=None) -> None:
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(ggrn_inputs.WORKLOADS), default="mamba2_prefill")
+    ap.add_argument("--workload", choices=sorted(ggrn_inputs.WORKLOADS), default="strided_odd_span")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -710,6 +814,11 @@ def main(argv=None) -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload (no per_config block)")
+    ap.add_argument("--profile-range", type=int, default=0,
+                    help="N launches between profiler start/stop for an ncu range capture "
+                         "(prints one short line; not the benchmark line)")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip timing the unfused PyTorch op chain (context)")
     ap.add_argument("--rows-sweep", default="",
@@ -721,7 +830,9 @@ def main(argv=None) -> None:
     _, world, _ = dist_env()
     if world != args.gpus and args.gpus != 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
-    if args.rows_sweep:
+    if args.profile_range:
+        run_profile_range(args)
+    elif args.rows_sweep:
         if args.steps > 2000:
             args.steps = 1000
         run_rows_sweep(args)
