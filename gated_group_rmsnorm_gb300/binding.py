@@ -31,8 +31,8 @@ MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create",
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
            "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc",
-           "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_host_workspace_bytes",
-           "ggrn_selftest_wait_timeout")
+           "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_forward_inproj_host",
+           "ggrn_host_workspace_bytes", "ggrn_selftest_wait_timeout")
 
 
 class GgrnError(RuntimeError):
@@ -92,6 +92,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ggrn_forward_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci,
                                         vp, i64, vp]
         L.ggrn_forward_host.restype = ci
+        L.ggrn_forward_inproj_host.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f,
+                                               ci, ci, vp, i64, vp]
+        L.ggrn_forward_inproj_host.restype = ci
         L.ggrn_host_workspace_bytes.argtypes = [i64, i64, ci]
         L.ggrn_host_workspace_bytes.restype = i64
         L.ggrn_forward_inproj.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f, ci, ci,
@@ -159,6 +162,14 @@ def ggrn_forward_host(y, gate, w, out, rows, width, group_size, y_row_stride, ga
     return load().ggrn_forward_host(y, gate, w, out, rows, width, group_size, y_row_stride,
                                     gate_row_stride, out_row_stride, eps, dtype, mode, workspace,
                                     workspace_bytes, stream)
+
+
+def ggrn_forward_inproj_host(inproj, inproj_row_stride, y_col, gate_col, w, out, out_row_stride,
+                             rows, width, group_size, eps, dtype, mode, workspace,
+                             workspace_bytes, stream) -> int:
+    return load().ggrn_forward_inproj_host(inproj, inproj_row_stride, y_col, gate_col, w, out,
+                                           out_row_stride, rows, width, group_size, eps, dtype,
+                                           mode, workspace, workspace_bytes, stream)
 
 
 def ggrn_forward_noalloc(y, gate, w, out, rows, width, group_size, y_row_stride,
@@ -356,13 +367,46 @@ def forward_host(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_
         workspace = host_workspace(rows, width, y.dtype, w.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    packed = _packed_pair(y, gate, rows, width, ys, gts)
     with torch.cuda.device(w.device):
-        st = ggrn_forward_host(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows,
-                               width, group_size, ys, gts, os_, float(eps), DTYPE_CODE[y.dtype], m,
-                               ws_ptr, ws_bytes, _stream_handle(w.device))
+        if packed is not None:
+            # y and gate are column ranges of one tensor's rows: declared as
+            # one packed matrix (the copy route may then move both at once)
+            base, ycol, gcol = packed
+            st = ggrn_forward_inproj_host(base, ys, ycol, gcol, w.data_ptr(), out.data_ptr(),
+                                          os_, rows, width, group_size, float(eps),
+                                          DTYPE_CODE[y.dtype], m, ws_ptr, ws_bytes,
+                                          _stream_handle(w.device))
+        else:
+            st = ggrn_forward_host(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(),
+                                   rows, width, group_size, ys, gts, os_, float(eps),
+                                   DTYPE_CODE[y.dtype], m, ws_ptr, ws_bytes,
+                                   _stream_handle(w.device))
     if st != OK:
         raise GgrnError(st, "ggrn_forward_host")
     return out
+
+
+def _packed_pair(y, gate, rows, width, ys, gts):
+    """(base pointer, y column, gate column) when y and gate are two column
+    ranges of the same rows of one tensor's storage, which holds every row
+    from the earlier range's first column to the later range's last one;
+    else None."""
+    if rows < 2 or ys != gts:
+        return None
+    if y.untyped_storage().data_ptr() != gate.untyped_storage().data_ptr():
+        return None
+    es = y.element_size()
+    yp, gp = y.data_ptr(), gate.data_ptr()
+    base = min(yp, gp)
+    ycol, gcol = (yp - base) // es, (gp - base) // es
+    if (yp - base) % es or (gp - base) % es or max(ycol, gcol) + width > ys:
+        return None
+    st0 = y.untyped_storage().data_ptr()
+    end = base + ((rows - 1) * ys + max(ycol, gcol) + width) * es
+    if base < st0 or end > st0 + y.untyped_storage().nbytes():
+        return None
+    return base, ycol, gcol
 
 
 class DecodeGraph:

@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["ggrn_api.cu", "ggrn_host.cu", "ggrn_kernels_bf16.cu", "ggrn_kernels_f16.cu",
            "ggrn_kernels_f32.cu"]
-HEADERS = ["ggrn_internal.h", "ggrn_kernels.cuh", "ggrn_stream.cuh"]
+HEADERS = ["ggrn_internal.h", "ggrn_kernels.cuh", "ggrn_slots.h", "ggrn_stream.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

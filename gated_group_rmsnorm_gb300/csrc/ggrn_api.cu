@@ -20,16 +20,18 @@
 
 #include "../../include/ggrn.h"
 #include "ggrn_internal.h"
+#include "ggrn_slots.h"
 
 // Device status word of the library (one per device): kernels whose bounded
 // waits run out set bits here (see ggrn_fault_status).
 __device__ unsigned int g_ggrn_fault;
 
 // Unit-claim words of the streaming kernel's dynamic schedule (epoch << 32 |
-// next unit; see claim_resolve).  Launches take the slots round robin, so
-// launches running at the same time on different streams normally use
-// different words; when two do share one, the epochs keep both complete.
-// Zero (epoch 0, never given to a launch) at module load.
+// next unit; see claim_resolve).  The host gives each word to one running
+// launch at a time (ggrn_slots.h: launches of one stream share a word, a word
+// passes to another stream once its last launch there has completed, and a
+// launch that finds none free takes the static schedule).  Zero (epoch 0,
+// never given to a launch) at module load.
 constexpr int kSchedSlots = 64;
 // Claimed indices are 32-bit: larger launches take the static schedule.
 constexpr int64_t kMaxClaimUnits = int64_t{1} << 30;
@@ -69,6 +71,33 @@ unsigned long long* sched_words() {
     cache[dev] = static_cast<unsigned long long*>(ptr);
   }
   return cache[dev];
+}
+
+// Ownership of the claim words of one device (see ggrn_slots.h): the stream
+// of each word's last launch and an event recorded after it.
+struct SlotTable {
+  std::mutex mu;
+  ClaimSlot slot[kSchedSlots];
+  cudaEvent_t ev[kSchedSlots] = {};
+  unsigned next = 0;
+};
+
+// Has the launch behind a slot's event completed?  A query that finds it
+// still running reports cudaErrorNotReady, which the runtime also keeps as
+// the thread's last error: that is cleared again, and a query is not made
+// while an earlier error is pending (it stays for the caller to read).
+bool slot_done(cudaEvent_t ev) {
+  if (!ev || cudaPeekAtLastError() != cudaSuccess) return false;
+  const cudaError_t q = cudaEventQuery(ev);
+  if (q == cudaErrorNotReady) cudaGetLastError();
+  return q == cudaSuccess;
+}
+
+SlotTable* slot_table() {
+  static SlotTable tables[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  return &tables[dev];
 }
 
 // A new claim epoch per launch (nonzero; wraps after 2^32 - 1 launches).
@@ -650,20 +679,36 @@ int launch(const Args& a, const Plan& plan, cudaStream_t s) {
   if (plan.grid == 0) return GGRN_OK;
   Plan p = plan;
   KParams k = make_params(a, p);
+  SlotTable* table = nullptr;
+  std::unique_lock<std::mutex> hold;  // held from the slot's choice to its event
+  int slot = -1;
   if (p.path == kStream) {
     k.fault = fault_word();
     if (!k.fault) return GGRN_ERR_CUDA;
     // A graph replays its launches with the parameters they were recorded
     // with, the claim epoch included: recorded launches take the static
     // schedule.
-    if (capturing(s) || p.items > kMaxClaimUnits) {
-      p.grid = p.grid_static;
-    } else {
+    if (!capturing(s) && p.items <= kMaxClaimUnits) {
       unsigned long long* words = sched_words();
-      if (!words) return GGRN_ERR_CUDA;
-      k.epoch = next_epoch();
-      k.sched = words + (k.epoch % kSchedSlots);
+      table = slot_table();
+      if (!words || !table) return GGRN_ERR_CUDA;
+      hold = std::unique_lock<std::mutex>(table->mu);
+      const uintptr_t sid = reinterpret_cast<uintptr_t>(s);
+      slot = pick_claim_slot(table->slot, kSchedSlots, sid, s == cudaStreamPerThread,
+                             table->next, [&](int i) { return slot_done(table->ev[i]); });
+      if (slot >= 0 && !table->ev[slot] &&
+          cudaEventCreateWithFlags(&table->ev[slot], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        table->ev[slot] = nullptr;
+        slot = -1;
+      }
+      if (slot >= 0) {
+        table->next = static_cast<unsigned>(slot + 1) % kSchedSlots;
+        k.epoch = next_epoch();
+        k.sched = words + slot;
+      }
     }
+    if (slot < 0) p.grid = p.grid_static;
   }
   cudaError_t e;
   switch (a.dtype) {
@@ -674,6 +719,20 @@ int launch(const Args& a, const Plan& plan, cudaStream_t s) {
   if (e != cudaSuccess) {
     tl_last_cuda_error = e;
     return GGRN_ERR_CUDA;
+  }
+  if (slot >= 0) {
+    // the slot is this stream's until the event after its launch completes;
+    // should the record fail, the slot counts as busy until a later record
+    // on it succeeds
+    table->slot[slot].owner = reinterpret_cast<uintptr_t>(s);
+    table->slot[slot].used = true;
+    e = cudaEventRecord(table->ev[slot], s);
+    if (e != cudaSuccess) {
+      cudaEventDestroy(table->ev[slot]);
+      table->ev[slot] = nullptr;
+      tl_last_cuda_error = e;
+      return GGRN_ERR_CUDA;
+    }
   }
   return GGRN_OK;
 }

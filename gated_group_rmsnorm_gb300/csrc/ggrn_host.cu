@@ -166,16 +166,22 @@ extern "C" int64_t ggrn_host_workspace_bytes(int64_t rows, int64_t width, int dt
   return kSlots * 3 * align_up(target_chunk_rows(rows, width, es) * width * es);
 }
 
-extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w,
-                                 void* out_host, int64_t rows, int64_t width,
-                                 int64_t group_size, int64_t y_row_stride,
-                                 int64_t gate_row_stride, int64_t out_row_stride, float eps,
-                                 int dtype, int mode, void* workspace, int64_t workspace_bytes,
-                                 void* cuda_stream) {
-  // The host matrices get the checks of ggrn_forward (shapes, dtype, NULL,
-  // element alignment, out overlapping y or gate).
-  const Args a = call_args(y_host, gate_host, w, out_host, rows, width, group_size, y_row_stride,
-                           gate_row_stride, out_row_stride, eps, dtype, mode);
+namespace ggrn {
+namespace {
+
+// The host entry points' common body.  `packed`: the caller declared y and
+// gate to be two column ranges of one packed host matrix (the fused in-proj
+// layout), so the bytes between and around the two ranges of each row, up
+// to the end of the later range, belong to that matrix and may be copied.
+int forward_host_impl(const Args& a, bool packed, void* workspace, int64_t workspace_bytes,
+                      cudaStream_t caller) {
+  const void* y_host = a.y;
+  const void* gate_host = a.gate;
+  const void* w = a.w;
+  void* out_host = a.out;
+  const int64_t rows = a.rows, width = a.width, group_size = a.gs;
+  const float eps = a.eps;
+  const int dtype = a.dtype, mode = a.mode;
   int st = validate_call(a);
   if (st != GGRN_OK || rows == 0) return st;
   // Pinned, mapped host buffers: one kernel on the caller's stream reads y
@@ -187,7 +193,7 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
   if (matrix_maps_in_place(y_host, rows, width, a.ys, es) &&
       matrix_maps_in_place(gate_host, rows, width, a.gts, es) &&
       matrix_maps_in_place(out_host, rows, width, a.os, es))
-    return forward_in_place(a, static_cast<cudaStream_t>(cuda_stream));
+    return forward_in_place(a, caller);
   if (!workspace) return GGRN_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return GGRN_ERR_ALIGN;
   const int64_t row_bytes = width * es;
@@ -198,17 +204,20 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
   while (chunk > 0 && kSlots * 3 * align_up(chunk * row_bytes) > workspace_bytes) --chunk;
   if (chunk < 1) return GGRN_ERR_ARG;
   const int64_t part = align_up(chunk * row_bytes);  // one tensor of one slot
-  // y and gate as two column ranges of one packed host matrix (a fused
-  // in-proj output) that cover at least 90 % of its rows: one contiguous
-  // copy per chunk, from the first used byte of its first row to the last
-  // used byte of its last row, into the slot's y and gate parts together;
-  // the kernel then reads the two ranges in place.
+  // y and gate declared as two column ranges of one packed host matrix (a
+  // fused in-proj output) that cover at least 90 % of its rows: one
+  // contiguous copy per chunk, from the first used byte of its first row to
+  // the last used byte of its last row, into the slot's y and gate parts
+  // together; the kernel then reads the two ranges in place.  Two separate
+  // matrices are never copied that way: the bytes between them need not be
+  // anyone's memory.
   const char* yb = static_cast<const char*>(y_host);
   const char* gb = static_cast<const char*>(gate_host);
   const int64_t pitch = a.ys * es;
   const char* lo = std::min(yb, gb);
   const int64_t span = (std::max(yb, gb) - lo) + row_bytes;  // used bytes of a row
-  bool joint = rows > 1 && a.ys == a.gts && span <= pitch && 10 * 2 * row_bytes >= 9 * pitch;
+  bool joint = packed && rows > 1 && a.ys == a.gts && span <= pitch &&
+               10 * 2 * row_bytes >= 9 * pitch;
   if (joint) {
     chunk = std::min(chunk, (2 * part - span) / pitch + 1);  // (n - 1) * pitch + span <= 2 * part
     joint = chunk >= 1;
@@ -226,7 +235,6 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
     record_cuda_error(e);
     return GGRN_ERR_CUDA;
   }
-  const cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
   // everything enqueued so far on the caller's stream comes first
   e = cudaEventRecord(hp->start, caller);
   for (cudaStream_t s : {hp->h2d, hp->comp, hp->d2h})
@@ -289,4 +297,43 @@ extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, cons
     return GGRN_ERR_CUDA;
   }
   return st;
+}
+
+}  // namespace
+}  // namespace ggrn
+
+extern "C" int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w,
+                                 void* out_host, int64_t rows, int64_t width,
+                                 int64_t group_size, int64_t y_row_stride,
+                                 int64_t gate_row_stride, int64_t out_row_stride, float eps,
+                                 int dtype, int mode, void* workspace, int64_t workspace_bytes,
+                                 void* cuda_stream) {
+  // The host matrices get the checks of ggrn_forward (shapes, dtype, NULL,
+  // element alignment, out overlapping y or gate).
+  const Args a = call_args(y_host, gate_host, w, out_host, rows, width, group_size, y_row_stride,
+                           gate_row_stride, out_row_stride, eps, dtype, mode);
+  return forward_host_impl(a, /*packed=*/false, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(cuda_stream));
+}
+
+extern "C" int ggrn_forward_inproj_host(const void* inproj_host, int64_t inproj_row_stride,
+                                        int64_t y_col, int64_t gate_col, const void* w,
+                                        void* out_host, int64_t out_row_stride, int64_t rows,
+                                        int64_t width, int64_t group_size, float eps, int dtype,
+                                        int mode, void* workspace, int64_t workspace_bytes,
+                                        void* cuda_stream) {
+  if (rows < 0 || width <= 0) return GGRN_ERR_SHAPE;
+  if (rows == 0) return GGRN_OK;
+  if (!inproj_host) return GGRN_ERR_NULL;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GGRN_ERR_DTYPE;
+  if (y_col < 0 || gate_col < 0 || y_col > inproj_row_stride - width ||
+      gate_col > inproj_row_stride - width)
+    return GGRN_ERR_SHAPE;
+  const int es = es_of(dtype);
+  const char* base = static_cast<const char*>(inproj_host);
+  const Args a = call_args(base + y_col * es, base + gate_col * es, w, out_host, rows, width,
+                           group_size, inproj_row_stride, inproj_row_stride, out_row_stride, eps,
+                           dtype, mode);
+  return forward_host_impl(a, /*packed=*/true, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(cuda_stream));
 }

@@ -186,6 +186,31 @@ int ggrn_forward_host(const void* y_host, const void* gate_host, const void* w, 
                       int64_t gate_row_stride, int64_t out_row_stride, float eps, int dtype,
                       int mode, void* workspace, int64_t workspace_bytes, void* cuda_stream);
 
+/*
+ * ggrn_forward_inproj_host -- ggrn_forward_host on y and gate given as two
+ * column ranges of one packed HOST matrix, the output of a fused input
+ * projection ("gated_group_rmsnorm" page, Parallelization: the y/gate views
+ * split from the fused in-proj).
+ *   inproj_host       : const T*, host, rows of inproj_row_stride elements;
+ *                       y is columns [y_col, y_col + width), gate columns
+ *                       [gate_col, gate_col + width).  The caller declares
+ *                       the whole of every row up to the end of the later
+ *                       range part of this one matrix: the copy route may
+ *                       then move y and gate of a chunk as one contiguous
+ *                       copy (columns between the ranges included, and never
+ *                       used), which ggrn_forward_host never does for two
+ *                       separately given matrices.
+ *   inproj_row_stride, y_col, gate_col : as in ggrn_forward_inproj.
+ *   other arguments   : as in ggrn_forward_host.
+ * Returns the ggrn_forward_host statuses; GGRN_ERR_SHAPE also when a column
+ * range leaves the row.
+ */
+int ggrn_forward_inproj_host(const void* inproj_host, int64_t inproj_row_stride, int64_t y_col,
+                             int64_t gate_col, const void* w, void* out_host,
+                             int64_t out_row_stride, int64_t rows, int64_t width,
+                             int64_t group_size, float eps, int dtype, int mode, void* workspace,
+                             int64_t workspace_bytes, void* cuda_stream);
+
 /* Device workspace in bytes for which ggrn_forward_host uses full-size
  * chunks (about 32 MB of y and gate per chunk, three slots); 0 for rows <= 0
  * or width <= 0. */

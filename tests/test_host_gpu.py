@@ -9,6 +9,7 @@ import torch
 
 import ggrn_inputs
 import gated_group_rmsnorm_gb300 as g
+from gated_group_rmsnorm_gb300 import binding
 from tests import gpu_util
 from tests.tolerance import ulp_dist
 
@@ -104,6 +105,28 @@ def test_packed_host_buffers(pw, ycol, gcol, pinned):
     host = ggrn_inputs.Inputs(y=y.contiguous(), gate=gate.contiguous(), w=w)
     res = gpu_util.compare(out, host, gs, 1e-5, 0)
     assert res["ok"], res
+
+
+def test_undeclared_packed_views_copy_separately():
+    """Two ranges of one pageable matrix given to ggrn_forward_host as two
+    matrices (not declared packed): copied one range at a time, never with
+    the bytes between them, and the same bits as the declared route."""
+    rows, width, gs = 333, 4800, 100
+    gen = torch.Generator().manual_seed(77)
+    packed = torch.randn(rows, 9664, generator=gen).to(torch.bfloat16)
+    w = (1.0 + 0.1 * torch.randn(width, generator=gen)).cuda()
+    y, gate = packed[:, :width], packed[:, width:2 * width]
+    ws = g.host_workspace(rows, width, torch.bfloat16, "cuda")
+    declared = g.forward_host(y, gate, w, group_size=gs, eps=1e-5, workspace=ws)
+    out = torch.empty((rows, width), dtype=torch.bfloat16)
+    st = g.ggrn_forward_host(y.data_ptr(), gate.data_ptr(), w.data_ptr(), out.data_ptr(), rows,
+                             width, gs, 9664, 9664, width, 1e-5, binding.DTYPE_CODE[y.dtype], 0,
+                             ws.data_ptr(), ws.numel(), binding._stream_handle(w.device))
+    assert st == binding.OK
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), declared.view(torch.int16))
+    host = ggrn_inputs.Inputs(y=y.contiguous(), gate=gate.contiguous(), w=w.cpu())
+    gpu_util.compare(out, host, gs, 1e-5, 0)
 
 
 def test_route_by_host_memory():

@@ -104,8 +104,8 @@ def test_two_streams_at_once():
 
 
 def test_many_launches_cycle_the_claim_words():
-    """More launches than claim words: every word is reused by later
-    launches, each of which replaces the previous launch's epoch."""
+    """More launches than claim words on one stream: the stream keeps one
+    word, and each launch replaces the previous launch's epoch in it."""
     g.fault_status(clear=True)
     wl, _, dev = _case("mamba2_prefill", 700, seed=3)
     ref = _fwd(wl, dev)
@@ -115,6 +115,28 @@ def test_many_launches_cycle_the_claim_words():
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(_bits(o), _bits(ref))
+    assert g.fault_status() == 0
+
+
+def test_more_streams_than_claim_words():
+    """Launches on more streams than there are claim words, all in flight at
+    once: each running launch gets a word of its own or, when every word is
+    held by another stream's running launch, the static schedule; every
+    output is the same bits."""
+    g.fault_status(clear=True)
+    wl, _, dev = _case("mamba2_prefill", 700, seed=4)
+    ref = _fwd(wl, dev)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(70)]
+    outs = [[torch.empty_like(ref) for _ in range(3)] for _ in streams]
+    for k in range(3):
+        for st, o in zip(streams, outs):
+            with torch.cuda.stream(st):
+                _fwd(wl, dev, out=o[k])
+    torch.cuda.synchronize()
+    for o in outs:
+        for x in o:
+            assert torch.equal(_bits(x), _bits(ref))
     assert g.fault_status() == 0
 
 
