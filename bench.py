@@ -668,6 +668,80 @@ def run_profile_range(args) -> None:
                       "csrc_sha": kernel_source_hash()}), flush=True)
 
 
+def run_timeline(args) -> None:
+    """Per-CTA timeline of N back-to-back launches of the workload, from the
+    profiling build (libggrn_timeline.so, include/ggrn_timeline.h): where a
+    launch's time goes besides moving its bytes.  One JSON line of medians
+    over the launches after the first three: the period between dependency
+    releases, the gap from the last CTA's end to the next release, when the
+    first stage reaches the consumers, the spread of the CTAs' ends and the
+    mean idle time of an SM at the tail."""
+    from gated_group_rmsnorm_gb300 import build as gbuild
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    L = ctypes.CDLL(gbuild.build(timeline=True))
+    i64, vp, f, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    L.ggrn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, ci, ci, vp]
+    L.ggrn_forward.restype = ci
+    wl = ggrn_inputs.WORKLOADS[args.workload]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
+    tname = IO_DTYPE[wl.dtype]
+    read, clear = getattr(L, f"ggrn_timeline_read_{tname}"), getattr(L, f"ggrn_timeline_clear_{tname}")
+    n = min(args.timeline, 60)
+    n_sets = max(2, -(-4 * L2_BYTES // wl.algorithmic_bytes()))
+    sets = [ggrn_inputs.make_inputs(wl, device=device, seed=s) for s in range(n_sets)]
+    outs = [torch.empty((wl.rows, wl.width), dtype=wl.dtype, device=device) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(device)
+    from gated_group_rmsnorm_gb300 import binding
+    raw = [_raw_args(binding, st, o, wl, ctypes.c_void_p(stream.cuda_stream))
+           for st, o in zip(sets, outs)]
+    for i in range(max(args.warmup, 3)):
+        assert L.ggrn_forward(*raw[i % n_sets]) == 0
+    torch.cuda.synchronize()
+    assert clear() == 0
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        L.ggrn_forward(*raw[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_event = e0.elapsed_time(e1) * 1e3 / n
+    buf = (ctypes.c_ulonglong * (64 * 320 * 5))()
+    assert read(buf) == 0
+    launches = []
+    for e in range(64):
+        ctas = [tuple(buf[(e * 320 + b) * 5 + k] for k in range(5)) for b in range(320)]
+        ctas = [c for c in ctas if c[1]]
+        if ctas:
+            launches.append(ctas)
+    launches.sort(key=lambda c: min(x[1] for x in c))
+    per = []
+    for i, c in enumerate(launches[:-1]):
+        rel = min(x[1] for x in c)
+        ends = sorted(x[3] for x in c)
+        firsts = sorted(x[2] - rel for x in c)
+        nrel = min(x[1] for x in launches[i + 1])
+        per.append({"period": nrel - rel, "busy": ends[-1] - rel, "gap": nrel - ends[-1],
+                    "first_min": firsts[0], "first_med": firsts[len(firsts) // 2],
+                    "first_max": firsts[-1], "end_spread": ends[-1] - ends[0],
+                    "tail_idle_mean": statistics.mean(ends[-1] - x for x in ends),
+                    "entry_early": rel - min(x[0] for x in c),
+                    "units": (min(x[4] for x in c), max(x[4] for x in c))})
+    per = per[3:]
+    med = {k: round(statistics.median(p[k] for p in per) / 1e3, 3) for k in per[0] if k != "units"}
+    print(json.dumps({"workload": wl.name, "rows": wl.rows, "launches": len(per),
+                      "event_us_per_launch": round(us_event, 3),
+                      "bytes_at_event_rate_gbs": round(wl.algorithmic_bytes() / us_event / 1e3, 1),
+                      "median_us": med, "units_per_cta_min_max": per[0]["units"],
+                      "ctas": len(launches[0]), "csrc_sha": kernel_source_hash(),
+                      "note": "global-timer stamps per CTA (profiling build); period = release "
+                              "to next release, gap = last CTA end to next release, first_* = "
+                              "first stage seen after release, tail_idle_mean = mean over CTAs "
+                              "of (last end - own end)"}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # Reference arm: the CPU oracle.
 # ---------------------------------------------------------------------------
@@ -816,6 +890,9 @@ def main(argv=None) -> None:
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the headline workload (no per_config block)")
+    ap.add_argument("--timeline", type=int, default=0,
+                    help="N launches through the profiling build: per-CTA timeline summary "
+                         "(not the benchmark line)")
     ap.add_argument("--profile-range", type=int, default=0,
                     help="N launches between profiler start/stop for an ncu range capture "
                          "(prints one short line; not the benchmark line)")
@@ -830,7 +907,9 @@ def main(argv=None) -> None:
     _, world, _ = dist_env()
     if world != args.gpus and args.gpus != 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
-    if args.profile_range:
+    if args.timeline:
+        run_timeline(args)
+    elif args.profile_range:
         run_profile_range(args)
     elif args.rows_sweep:
         if args.steps > 2000:

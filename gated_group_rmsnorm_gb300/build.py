@@ -20,6 +20,10 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libggrn.so")
 BUILD_DIR = os.path.join(HERE, "_build")
+# profiling build: the same library with the streaming kernels' per-CTA
+# timeline compiled in (-DGGRN_TIMELINE); never loaded by the product path
+TIMELINE_LIB_PATH = os.path.join(HERE, "libggrn_timeline.so")
+TIMELINE_BUILD_DIR = os.path.join(HERE, "_build_timeline")
 
 SOURCES = ["ggrn_api.cu", "ggrn_host.cu", "ggrn_kernels_bf16.cu", "ggrn_kernels_f16.cu",
            "ggrn_kernels_f32.cu"]
@@ -51,16 +55,22 @@ def _deps() -> list[str]:
             [os.path.join(INCLUDE, "ggrn.h"), os.path.abspath(__file__)])
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> str:
-    """Compile and link ``libggrn.so``; return its path.  No-op when up to date."""
-    if not force and not ptxas_verbose and not _stale(LIB_PATH, _deps()):
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True,
+          timeline: bool = False) -> str:
+    """Compile and link ``libggrn.so`` (``timeline``: the profiling build
+    ``libggrn_timeline.so``); return its path.  No-op when up to date."""
+    lib_path = TIMELINE_LIB_PATH if timeline else LIB_PATH
+    build_dir = TIMELINE_BUILD_DIR if timeline else BUILD_DIR
+    if not force and not ptxas_verbose and not _stale(lib_path, _deps()):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if timeline:
+        extra += ["-DGGRN_TIMELINE"]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-c", os.path.join(CSRC, src),
                "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -73,18 +83,21 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
     if ptxas_verbose or not quiet:
         for _, log in results:
             sys.stdout.write(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-v", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="the profiling build with the per-CTA timeline (libggrn_timeline.so)")
     args = ap.parse_args()
-    print(build(force=args.force, ptxas_verbose=args.ptxas_v, quiet=False))
+    print(build(force=args.force, ptxas_verbose=args.ptxas_v, quiet=False,
+                timeline=args.timeline))

@@ -8,3 +8,18 @@ cudaError_t launch_f16(const KParams& k, const Plan& p, int mode, cudaStream_t s
   return cudaErrorInvalidValue;
 }
 }  // namespace ggrn
+
+#ifdef GGRN_TIMELINE
+// Profiling build only: the timeline stamps of this element type's streaming
+// launches (see ggrn_stream.cuh), copied to `host` (64 x 320 x 5 uint64), and
+// cleared.
+extern "C" int ggrn_timeline_read_f16(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_ggrn_timeline, sizeof(g_ggrn_timeline)) == cudaSuccess ? 0
+                                                                                             : 1;
+}
+extern "C" int ggrn_timeline_clear_f16(void) {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_ggrn_timeline) != cudaSuccess) return 1;
+  return cudaMemset(ptr, 0, sizeof(g_ggrn_timeline)) == cudaSuccess ? 0 : 1;
+}
+#endif

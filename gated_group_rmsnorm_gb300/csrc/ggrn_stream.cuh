@@ -33,6 +33,25 @@
 
 #include "ggrn_kernels.cuh"
 
+// Per-CTA timeline of streaming launches, compiled in only with
+// -DGGRN_TIMELINE (a separate profiling build of the library): for each of the
+// last 64 launches (by claim epoch) and each CTA, the global-timer stamps of
+// entry, release of the dependency wait, the first stage seen by consumer
+// warp 0 and the end of the CTA's last consumer warp, and the units it took.
+#ifdef GGRN_TIMELINE
+constexpr int kTimelineLaunches = 64;
+constexpr int kTimelineCtas = 320;
+static __device__ unsigned long long g_ggrn_timeline[kTimelineLaunches][kTimelineCtas][5];
+__device__ __forceinline__ unsigned long long timeline_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define GGRN_TIMELINE_AT(p, field) \
+  g_ggrn_timeline[(p).epoch % kTimelineLaunches][blockIdx.x][field]
+#define GGRN_TIMELINE_ON (blockIdx.x < kTimelineCtas)
+#endif
+
 namespace ggrn {
 
 // At most kWaitLimit polls, each suspending for at most ~kWaitHintNs: a wait
@@ -235,7 +254,20 @@ __device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned cha
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+#ifdef GGRN_TIMELINE
+  const unsigned long long t_entry = timeline_now();
+#endif
   pdl_wait();
+#ifdef GGRN_TIMELINE
+  if (threadIdx.x == 0 && GGRN_TIMELINE_ON) {
+    GGRN_TIMELINE_AT(p, 0) = t_entry;
+    GGRN_TIMELINE_AT(p, 1) = timeline_now();
+    GGRN_TIMELINE_AT(p, 2) = 0;
+    GGRN_TIMELINE_AT(p, 3) = 0;
+    GGRN_TIMELINE_AT(p, 4) = 0;
+  }
+  __syncthreads();
+#endif
   pdl_launch_dependents();
   return c;
 }
@@ -505,6 +537,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
       break;
     }
     const int64_t u = c.unit_of[s];
+#ifdef GGRN_TIMELINE
+    if (warp == 0 && lane == 0 && GGRN_TIMELINE_ON && u >= 0) {
+      if (GGRN_TIMELINE_AT(p, 4) == 0) GGRN_TIMELINE_AT(p, 2) = timeline_now();
+      GGRN_TIMELINE_AT(p, 4) += 1;
+    }
+#endif
     if (u < 0) break;
     const UnitPos up = unit_pos(p, u);
     const int nitems = static_cast<int>(up.ngroups / Q);
@@ -610,6 +648,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
+#ifdef GGRN_TIMELINE
+  if (lane == 0 && GGRN_TIMELINE_ON) atomicMax(&GGRN_TIMELINE_AT(p, 3), timeline_now());
+#endif
 }
 
 // Launch one instantiation, opting in to more than 48 KB of dynamic shared

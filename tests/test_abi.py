@@ -14,17 +14,27 @@ from gated_group_rmsnorm_gb300 import binding
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared_functions():
+def _declared_functions(header="ggrn.h"):
     names = set()
-    inc = os.path.join(ROOT, "include")
-    for fn in os.listdir(inc):
-        if not fn.endswith(".h"):
-            continue
-        src = open(os.path.join(inc, fn)).read()
-        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ggrn_\w+)\s*\(", src, flags=re.M):
-            names.add(m.group(1))
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ggrn_\w+)\s*\(", src, flags=re.M):
+        names.add(m.group(1))
     return names
+
+
+def test_every_header_is_checked():
+    assert sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")) == \
+        ["ggrn.h", "ggrn_timeline.h"]
+
+
+def test_profiling_build_exports_its_symbols():
+    """The profiling build (libggrn_timeline.so) exports what ggrn_timeline.h
+    declares, besides every entry point of ggrn.h."""
+    from gated_group_rmsnorm_gb300 import build as gbuild
+    tl = ctypes.CDLL(gbuild.build(timeline=True))
+    for name in _declared_functions("ggrn_timeline.h") | _declared_functions("ggrn.h"):
+        assert hasattr(tl, name), f"{name} not exported by the profiling build"
 
 
 @pytest.fixture(scope="module")
