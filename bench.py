@@ -298,6 +298,56 @@ def _decode_numbers(g, device) -> dict:
             "note": "max(device time, host wall time) per call over back-to-back calls"}
 
 
+def _outproj_numbers(g, device, steps: int, d_models=(3840, 7680)) -> dict:
+    """The norm fused into the out_proj GEMM (ggrn_norm_outproj) on the
+    Mamba-2 prefill shape, against the same two steps unfused: the norm
+    kernel (ggrn_forward) then torch.matmul (cuBLAS) on its output; and the
+    GEMM alone.  µs per step from CUDA events over `steps` back-to-back
+    steps after warm-up; TFLOP/s = 2 M N K / time."""
+    wl = ggrn_inputs.WORKLOADS["mamba2_prefill"]
+    inp = ggrn_inputs.make_inputs(wl, device=device)
+    out = {}
+    for d_model in d_models:
+        w_out = ggrn_inputs.make_outproj_weight(d_model, wl.width, device=device, seed=1)
+        z = torch.empty((wl.rows, d_model), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(max(16, g.load().ggrn_norm_outproj_workspace_bytes(
+            wl.rows, wl.width, wl.group_size)), dtype=torch.uint8, device=device)
+        a = torch.empty((wl.rows, wl.width), dtype=torch.bfloat16, device=device)
+
+        def fused():
+            g.norm_outproj(inp.y, inp.gate, inp.w, w_out, group_size=wl.group_size, eps=wl.eps,
+                           out=z, workspace=ws)
+
+        def unfused():
+            g.forward(inp.y, inp.gate, inp.w, group_size=wl.group_size, eps=wl.eps, out=a)
+            torch.matmul(a, w_out.T, out=z)
+
+        def gemm_only():
+            torch.matmul(a, w_out.T, out=z)
+
+        res = {}
+        for name, fn in (("fused", fused), ("unfused_norm_then_cublas", unfused),
+                         ("cublas_gemm_only", gemm_only)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / steps
+            res[name] = {"us": round(us, 2),
+                         "tflops": round(2.0 * wl.rows * d_model * wl.width / us / 1e6, 1)}
+        res["fused_vs_unfused"] = round(res["unfused_norm_then_cublas"]["us"] / res["fused"]["us"],
+                                        3)
+        out[f"d_model_{d_model}"] = res
+        del w_out, z, ws, a
+    return {"workload": "mamba2_prefill (4096 x 7680, groups of 960) -> out_proj [d_model, 7680], "
+                        "bf16, f32 sums", "steps": steps, **out}
+
+
 def _cpu_baseline(wl, budget_s: float = 10.0) -> dict:
     """The single-threaded oracle on host cores: sample rows of the workload,
     repeated until the budget is spent."""
@@ -606,6 +656,8 @@ def run_ours(args) -> None:
         e2e["value"] = round(world * bytes_per_step / (e2e_ms / 1e3) / 1e9, 2)
         e2e["ms_per_step"] = round(e2e_ms, 4)
     decode = _decode_numbers(g, device) if (rank == 0 and not args.no_decode) else None
+    outproj = (_outproj_numbers(g, device, max(args.steps, 20))
+               if (rank == 0 and not args.no_outproj) else None)
     if rank == 0 and world == 1 and not args.no_unfused:
         extra["unfused_chain"] = _unfused_chain(wl, sets, min(args.steps, 200))
     del sets
@@ -634,6 +686,8 @@ def run_ours(args) -> None:
     line.update(extra)
     if decode is not None:
         line["decode"] = decode
+    if outproj is not None:
+        line["norm_outproj"] = outproj
     print(json.dumps(line), flush=True)
 
 
@@ -888,6 +942,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-outproj", action="store_true",
+                    help="skip timing the norm fused into the out_proj GEMM against the unfused pair")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the headline workload (no per_config block)")
     ap.add_argument("--timeline", type=int, default=0,

@@ -14,12 +14,13 @@ from .binding import (BF16, DTYPE_CODE, F16, F32, MAMBA2, ONNX, PATH_AUTO, PATH_
                       PATH_SCALAR, PATH_STRADDLE, PATH_STREAM, PATH_TEAM, PATH_WIDE, DecodeGraph,
                       GgrnError, fault_status, forward, forward_host, forward_inproj,
                       ggrn_forward, ggrn_forward_host, ggrn_forward_inproj,
-                      ggrn_forward_inproj_host, ggrn_forward_noalloc, ggrn_forward_path, ggrn_plan, host_workspace, library_path, load, plan,
+                      ggrn_forward_inproj_host, ggrn_forward_noalloc, ggrn_forward_path,
+                      ggrn_norm_outproj, norm_outproj, ggrn_plan, host_workspace, library_path, load, plan,
                       status_string)
 
 __all__ = ["forward", "forward_host", "forward_inproj", "plan", "DecodeGraph", "GgrnError",
            "ggrn_forward", "ggrn_forward_host", "ggrn_forward_inproj", "ggrn_forward_inproj_host",
-           "ggrn_forward_noalloc",
+           "ggrn_forward_noalloc", "ggrn_norm_outproj", "norm_outproj",
            "ggrn_forward_path", "ggrn_plan", "host_workspace", "load",
            "library_path", "status_string", "MAMBA2", "ONNX", "F32", "F16", "BF16", "PATH_AUTO", "PATH_TEAM", "PATH_WIDE", "PATH_STRADDLE", "PATH_SCALAR",
            "PATH_STREAM", "PATH_NAMES", "DTYPE_CODE", "fault_status"]

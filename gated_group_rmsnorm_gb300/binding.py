@@ -32,7 +32,8 @@ EXPORTS = ("ggrn_forward", "ggrn_forward_path", "ggrn_plan", "ggrn_graph_create"
            "ggrn_graph_launch", "ggrn_graph_destroy", "ggrn_status_string", "ggrn_version",
            "ggrn_fault_status", "ggrn_last_cuda_error", "ggrn_forward_noalloc",
            "ggrn_forward_inproj", "ggrn_forward_host", "ggrn_forward_inproj_host",
-           "ggrn_host_workspace_bytes", "ggrn_selftest_wait_timeout")
+           "ggrn_host_workspace_bytes", "ggrn_selftest_wait_timeout", "ggrn_norm_outproj",
+           "ggrn_norm_outproj_workspace_bytes")
 
 
 class GgrnError(RuntimeError):
@@ -95,6 +96,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ggrn_forward_inproj_host.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f,
                                                ci, ci, vp, i64, vp]
         L.ggrn_forward_inproj_host.restype = ci
+        L.ggrn_norm_outproj.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f, vp,
+                                        i64, vp, vp]
+        L.ggrn_norm_outproj.restype = ci
+        L.ggrn_norm_outproj_workspace_bytes.argtypes = [i64, i64, i64]
+        L.ggrn_norm_outproj_workspace_bytes.restype = i64
         L.ggrn_host_workspace_bytes.argtypes = [i64, i64, ci]
         L.ggrn_host_workspace_bytes.restype = i64
         L.ggrn_forward_inproj.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, i64, i64, f, ci, ci,
@@ -384,6 +390,50 @@ def forward_host(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, *, group_
                                    _stream_handle(w.device))
     if st != OK:
         raise GgrnError(st, "ggrn_forward_host")
+    return out
+
+
+def ggrn_norm_outproj(y, gate, w, w_out, z, rows, width, group_size, y_row_stride,
+                      gate_row_stride, d_model, eps, workspace, workspace_bytes, a_out,
+                      stream) -> int:
+    return load().ggrn_norm_outproj(y, gate, w, w_out, z, rows, width, group_size, y_row_stride,
+                                    gate_row_stride, d_model, eps, workspace, workspace_bytes,
+                                    a_out, stream)
+
+
+def norm_outproj(y: torch.Tensor, gate: torch.Tensor, w: torch.Tensor, w_out: torch.Tensor, *,
+                 group_size: int, eps: float, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None,
+                 a_out: torch.Tensor | None = None) -> torch.Tensor:
+    """The Mamba-2 norm fused into the out_proj GEMM (``ggrn_norm_outproj``):
+    ``out = norm(y, gate, w) @ w_out.T`` in bf16 with f32 sums, the norm's
+    output never written unless ``a_out`` (a [rows, width] bf16 tensor) is
+    given.  ``y``, ``gate``: bf16 CUDA [..., width] (row-strided views
+    allowed); ``w``: f32 [width]; ``w_out``: bf16 [d_model, width]
+    contiguous.  Enqueued on the current stream."""
+    if not (y.is_cuda and gate.is_cuda and w.is_cuda and w_out.is_cuda):
+        raise ValueError("norm_outproj takes CUDA tensors")
+    if y.dtype != torch.bfloat16 or gate.dtype != torch.bfloat16 or w_out.dtype != torch.bfloat16:
+        raise ValueError("norm_outproj takes bf16 y, gate and w_out")
+    width = y.shape[-1]
+    rows, ys = _as_rows(y, width, "y")
+    _, gts = _as_rows(gate, width, "gate")
+    w = w.reshape(width).to(torch.float32).contiguous()
+    if w_out.dim() != 2 or w_out.shape[1] != width or not w_out.is_contiguous():
+        raise ValueError("w_out must be a contiguous [d_model, width] tensor")
+    d_model = w_out.shape[0]
+    if out is None:
+        out = torch.empty(y.shape[:-1] + (d_model,), dtype=torch.bfloat16, device=y.device)
+    if workspace is None:
+        nbytes = load().ggrn_norm_outproj_workspace_bytes(rows, width, group_size)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=y.device)
+    st = ggrn_norm_outproj(y.data_ptr(), gate.data_ptr(), w.data_ptr(), w_out.data_ptr(),
+                           out.data_ptr(), rows, width, group_size, ys, gts, d_model, float(eps),
+                           workspace.data_ptr(), workspace.numel(),
+                           a_out.data_ptr() if a_out is not None else None,
+                           _stream_handle(y.device))
+    if st != OK:
+        raise GgrnError(st, "ggrn_norm_outproj")
     return out
 
 

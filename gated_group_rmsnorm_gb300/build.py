@@ -26,7 +26,7 @@ TIMELINE_LIB_PATH = os.path.join(HERE, "libggrn_timeline.so")
 TIMELINE_BUILD_DIR = os.path.join(HERE, "_build_timeline")
 
 SOURCES = ["ggrn_api.cu", "ggrn_host.cu", "ggrn_kernels_bf16.cu", "ggrn_kernels_f16.cu",
-           "ggrn_kernels_f32.cu"]
+           "ggrn_kernels_f32.cu", "ggrn_outproj.cu"]
 HEADERS = ["ggrn_internal.h", "ggrn_kernels.cuh", "ggrn_slots.h", "ggrn_stream.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

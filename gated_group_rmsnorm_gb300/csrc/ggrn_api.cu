@@ -783,6 +783,8 @@ int launch_plan(const Args& a, const Plan& p, cudaStream_t s) { return launch(a,
 
 void record_cuda_error(cudaError_t e) { tl_last_cuda_error = e; }
 
+unsigned int* device_fault_word() { return fault_word(); }
+
 KParams make_params(const Args& a, const Plan& p) {
   KParams k;
   k.y = a.y;

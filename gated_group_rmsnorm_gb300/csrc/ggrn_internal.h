@@ -142,6 +142,8 @@ int plan_family(const Args& a, int path, int vpl, Plan* p);
 int launch_plan(const Args& a, const Plan& p, cudaStream_t s);
 // Remember the CUDA error behind a GGRN_ERR_CUDA (ggrn_last_cuda_error).
 void record_cuda_error(cudaError_t e);
+// The current device's status word (bits of ggrn_fault_status), or NULL.
+unsigned int* device_fault_word();
 
 // Launchers, one per element type (defined in ggrn_kernels_<T>.cu).  They
 // enqueue the kernel the plan names with programmatic dependent launch

@@ -139,3 +139,15 @@ def random_case(rows: int, width: int, group_size: int, dtype: torch.dtype, mode
     wl = Workload(f"case_{rows}x{width}_g{group_size}", rows, width, group_size, dtype, mode,
                   1e-5, std=std, seed=seed)
     return make_inputs(wl, device=device)
+
+
+def make_outproj_weight(d_model: int, width: int, device: str | torch.device = "cpu",
+                        seed: int = 0) -> torch.Tensor:
+    """The out_proj weight that follows the norm (a Linear layer's
+    [d_model, width] matrix): N(0, 1/width) f32 draws from a generator seeded
+    with ``seed``, cast to bf16 with round-to-nearest-even."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    w = torch.randn((d_model, width), dtype=torch.float32, device=device, generator=g)
+    return (w * (1.0 / width ** 0.5)).to(torch.bfloat16)

@@ -211,6 +211,46 @@ int ggrn_forward_inproj_host(const void* inproj_host, int64_t inproj_row_stride,
                              int64_t group_size, float eps, int dtype, int mode, void* workspace,
                              int64_t workspace_bytes, void* cuda_stream);
 
+/*
+ * ggrn_norm_outproj -- the Mamba-2 gated group-RMSNorm fused into the A
+ * operand of the out_proj GEMM that follows it ("gated_group_rmsnorm" page,
+ * the paragraph after the math block: the norm returns the model dtype and
+ * the out_proj consumes it as it is):
+ *     A[m, k] = the norm's output (MAMBA2 semantics, bf16),
+ *     z[m, n] = cast_bf16( sum_k f32(A[m, k]) * f32(w_out[n, k]) )   (f32 sums)
+ * A is built tile by tile in shared memory and fed to the tensor cores; it is
+ * written to memory only when `a_out` is given.  Two kernels on `cuda_stream`:
+ * the per-group normalisers into `workspace`, then the GEMM.
+ *   y, gate       : const bf16*, DEVICE, [rows, width], row strides
+ *                   y_row_stride / gate_row_stride (elements, multiples of 8).
+ *   w             : const float*, DEVICE, [width] (the norm weight).
+ *   w_out         : const bf16*, DEVICE, [d_model, width] row-major (the
+ *                   out_proj weight as a Linear layer stores it).
+ *   z             : bf16*, DEVICE, [rows, d_model] contiguous.
+ *   workspace     : DEVICE, caller-owned, at least
+ *                   ggrn_norm_outproj_workspace_bytes(rows, width, group_size)
+ *                   bytes, 16-byte aligned (rows x groups floats).
+ *   a_out         : optional bf16*, DEVICE, [rows, width] contiguous: the
+ *                   normalised A as the GEMM used it (verification); NULL to
+ *                   skip.
+ * Shapes the kernel covers: rows a multiple of 128, width and group_size
+ * multiples of 64, d_model a multiple of 32 (split into tiles of 2 x N with
+ * N the largest multiple of 16 up to 256 that divides it); all pointers
+ * 16-byte aligned.  Returns GGRN_OK; GGRN_ERR_SHAPE / NULL / ALIGN / OVERLAP
+ * as ggrn_forward for y, gate and w, and for z, w_out, workspace and a_out;
+ * GGRN_ERR_ARG for a workspace too small; GGRN_ERR_UNSUPPORTED for shapes
+ * outside the above; GGRN_ERR_CUDA when a launch fails.  Allocates nothing;
+ * the device status word (ggrn_fault_status) gets bit 16 if a bounded wait
+ * of the GEMM ran out.
+ */
+int ggrn_norm_outproj(const void* y, const void* gate, const void* w, const void* w_out, void* z,
+                      int64_t rows, int64_t width, int64_t group_size, int64_t y_row_stride,
+                      int64_t gate_row_stride, int64_t d_model, float eps, void* workspace,
+                      int64_t workspace_bytes, void* a_out, void* cuda_stream);
+
+/* Workspace bytes ggrn_norm_outproj needs (0 for invalid shapes). */
+int64_t ggrn_norm_outproj_workspace_bytes(int64_t rows, int64_t width, int64_t group_size);
+
 /* Device workspace in bytes for which ggrn_forward_host uses full-size
  * chunks (about 32 MB of y and gate per chunk, three slots); 0 for rows <= 0
  * or width <= 0. */

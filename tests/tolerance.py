@@ -156,6 +156,21 @@ def onnx_flip(got: torch.Tensor, ref: torch.Tensor, pre: torch.Tensor,
     return near & (ulp_dist(got, tn) == 0)
 
 
+def mamba2_flip_mask(ref_t: torch.Tensor, pre: torch.Tensor, gate: torch.Tensor,
+                     group_size: int) -> torch.Tensor:
+    """Elements whose Mamba-2 intermediate t may flip on a correct kernel
+    (``pre`` within tau of a rounding midpoint, tau as in ``check``): the only
+    elements of a correct kernel's output that may differ from the oracle's."""
+    rows, width = ref_t.shape
+    b = gate.double().abs().clamp(max=SILU_ARG_CAP)
+    b = torch.where(torch.isnan(b), torch.full_like(b, SILU_ARG_CAP), b)
+    bmax = b.reshape(rows, width // group_size, group_size).amax(-1, keepdim=True)
+    tau = ((group_size + TAU_CONST) + b +
+           bmax.expand(rows, width // group_size, group_size).reshape(rows, width)) * U
+    _, near = flip_target(ref_t, pre, tau)
+    return near
+
+
 def f32_accept(got: torch.Tensor, ref: torch.Tensor, rtol: float = F32_RTOL,
                atol: float = F32_ATOL) -> torch.Tensor:
     g, r = got.double(), ref.double()
