@@ -942,6 +942,10 @@ def main(argv=None) -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--outproj-only", action="store_true",
+                    help="only the fused out_proj leg (its JSON block), for profiling")
+    ap.add_argument("--d-model", type=int, default=0,
+                    help="with --outproj-only: one out_proj width instead of 3840 and 7680")
     ap.add_argument("--no-outproj", action="store_true",
                     help="skip timing the norm fused into the out_proj GEMM against the unfused pair")
     ap.add_argument("--no-per-config", action="store_true",
@@ -963,7 +967,13 @@ def main(argv=None) -> None:
     _, world, _ = dist_env()
     if world != args.gpus and args.gpus != 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
-    if args.timeline:
+    if args.outproj_only:
+        import gated_group_rmsnorm_gb300 as g
+        torch.cuda.set_device(0)
+        g.load(build_if_missing=True)
+        dm = (args.d_model,) if args.d_model else (3840, 7680)
+        print(json.dumps(_outproj_numbers(g, torch.device("cuda", 0), args.steps, dm)), flush=True)
+    elif args.timeline:
         run_timeline(args)
     elif args.profile_range:
         run_profile_range(args)

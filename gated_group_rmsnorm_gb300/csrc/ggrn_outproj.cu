@@ -183,13 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* base = smem_raw + (base_u - raw_u);
   const uint32_t bar_u = base_u + kStages * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
-  // barriers: full_tma[2], full_a[2], empty[2], acc_full; then the TMEM
-  // address slot and the abort flag
-  auto full_tma = [&](int s) { return bar_u + 8u * s; };
-  auto full_a = [&](int s) { return bar_u + 8u * (2 + s); };
-  auto empty = [&](int s) { return bar_u + 8u * (4 + s); };
-  const uint32_t acc_full = bar_u + 8u * 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  // barriers: full_yg[2] (y and gate landed), full_b[2] (W_out landed),
+  // full_a[2] (A built; also: y and gate read), empty_b[2] (the MMAs of the
+  // stage done: A and B free), acc_full; then the TMEM address slot and the
+  // abort flag
+  auto full_yg = [&](int s) { return bar_u + 8u * s; };
+  auto full_b = [&](int s) { return bar_u + 8u * (2 + s); };
+  auto full_a = [&](int s) { return bar_u + 8u * (4 + s); };
+  auto empty_b = [&](int s) { return bar_u + 8u * (6 + s); };
+  const uint32_t acc_full = bar_u + 8u * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   auto sA = [&](int s) { return base_u + s * kStageBytes; };
   auto sB = [&](int s) { return base_u + s * kStageBytes + kABytes; };
@@ -202,13 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 2 * bnh;
   const int KB = static_cast<int>(p.K / kBK);
   const uint32_t b_half_bytes = static_cast<uint32_t>(bnh) * kBK * 2;
-  const uint32_t stage_tx = 2 * kYBytes + 2 * b_half_bytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_tma(s), 1);
+      mbar_init(full_yg(s), 1);
+      mbar_init(full_b(s), 1);
       mbar_init(full_a(s), kProducerThreads);
-      mbar_init(empty(s), 1);
+      mbar_init(empty_b(s), 1);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -224,28 +227,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
 
   if (warp == 0) {
-    // ---- copies: y, gate and the two W_out halves of each K block ----
-    if (lane == 0) {
+    // ---- copies: lane 0 y and gate (refilled once the A block is built
+    // from them), lane 1 the two W_out halves (refilled once the stage's
+    // MMAs are done) ----
+    if (lane < 2) {
+      const bool yg = lane == 0;
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(empty(s), static_cast<uint32_t>(kb / kStages - 1) & 1u)) {
+        const uint32_t prev = static_cast<uint32_t>(kb / kStages - 1) & 1u;
+        if (kb >= kStages && !mbar_wait(yg ? full_a(s) : empty_b(s), prev)) {
           *abort_flag = 1;
           atomicOr(p.fault, kFaultGemmWait);
           break;
         }
         if (*abort_flag) break;
         const int k0 = kb * kBK;
-        mbar_expect_tx(full_tma(s), stage_tx);
-        tma_load_2d(sY(s), &tm_y, k0, static_cast<int>(m0), full_tma(s));
-        tma_load_2d(sG(s), &tm_g, k0, static_cast<int>(m0), full_tma(s));
-        tma_load_2d(sB(s), &tm_b, k0, static_cast<int>(n0), full_tma(s));
-        tma_load_2d(sB(s) + b_half_bytes, &tm_b, k0, static_cast<int>(n0 + bnh), full_tma(s));
+        if (yg) {
+          mbar_expect_tx(full_yg(s), 2 * kYBytes);
+          tma_load_2d(sY(s), &tm_y, k0, static_cast<int>(m0), full_yg(s));
+          tma_load_2d(sG(s), &tm_g, k0, static_cast<int>(m0), full_yg(s));
+        } else {
+          mbar_expect_tx(full_b(s), 2 * b_half_bytes);
+          tma_load_2d(sB(s), &tm_b, k0, static_cast<int>(n0), full_b(s));
+          tma_load_2d(sB(s) + b_half_bytes, &tm_b, k0, static_cast<int>(n0 + bnh), full_b(s));
+        }
         issued = kb + 1;
       }
       // every issued copy lands before the CTA can leave
       for (int kb = issued - kStages < 0 ? 0 : issued - kStages; kb < issued; ++kb)
-        if (!mbar_wait(full_tma(kb % kStages), static_cast<uint32_t>(kb / kStages) & 1u))
+        if (!mbar_wait(yg ? full_yg(kb % kStages) : full_b(kb % kStages),
+                       static_cast<uint32_t>(kb / kStages) & 1u))
           atomicOr(p.fault, kFaultGemmWait);
     }
   } else if (warp == 1) {
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-        if (*abort_flag || !mbar_wait(full_tma(s), ph) || !mbar_wait(full_a(s), ph)) {
+        if (*abort_flag || !mbar_wait(full_a(s), ph) || !mbar_wait(full_b(s), ph)) {
           *abort_flag = 1;
           atomicOr(p.fault, kFaultGemmWait);
           break;
@@ -271,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem, a_desc + adv, b_desc0 + adv, idesc, kb > 0 || kk > 0);
           mma_bf16(tmem + kHalfCol, a_desc + adv, b_desc1 + adv, idesc, kb > 0 || kk > 0);
         }
-        mma_commit(empty(s));  // frees the stage once these MMAs have read it
+        mma_commit(empty_b(s));  // frees A and B of the stage once these MMAs have read them
       }
       mma_commit(acc_full);  // the accumulators are complete (or abandoned)
       // wait for it here too, so that no MMA still runs when TMEM is freed
@@ -283,22 +295,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rq = t >> 3;                // row within a group of 32 rows
     const int c = t & 7;                  // 16-byte chunk (8 columns) of the 64
     const float* w = p.w;
+    // the weight columns and normalisers of the next block are fetched one
+    // block ahead (their global-memory latency then overlaps this block)
+    float4 w_lo = __ldg(reinterpret_cast<const float4*>(w + 8 * c));
+    float4 w_hi = __ldg(reinterpret_cast<const float4*>(w + 8 * c + 4));
+    float nfv[kBM / 32];
+#pragma unroll
+    for (int i = 0; i < kBM / 32; ++i) nfv[i] = __ldg(p.nf + (m0 + rq + 32 * i) * p.G);
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % kStages;
-      if (*abort_flag || !mbar_wait(full_tma(s), static_cast<uint32_t>(kb / kStages) & 1u)) {
+      const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
+      // y and gate of this block landed; A[s] free (the MMAs of kb - 2 done)
+      if (*abort_flag || !mbar_wait(full_yg(s), ph) ||
+          (kb >= kStages && !mbar_wait(empty_b(s), ph ^ 1u))) {
         *abort_flag = 1;
         if (lane == 0) atomicOr(p.fault, kFaultGemmWait);
         break;
       }
       const int64_t k0 = static_cast<int64_t>(kb) * kBK;
-      const int64_t g = k0 / p.gs;  // a K block never crosses a group (gs % 64 == 0)
-      const float4 w_lo = __ldg(reinterpret_cast<const float4*>(w + k0 + 8 * c));
-      const float4 w_hi = __ldg(reinterpret_cast<const float4*>(w + k0 + 8 * c + 4));
       const float wv[8] = {w_lo.x, w_lo.y, w_lo.z, w_lo.w, w_hi.x, w_hi.y, w_hi.z, w_hi.w};
+      float nfc[kBM / 32];
+#pragma unroll
+      for (int i = 0; i < kBM / 32; ++i) nfc[i] = nfv[i];
+      if (kb + 1 < KB) {
+        const int64_t k1 = k0 + kBK;
+        const int64_t g1 = k1 / p.gs;  // a K block never crosses a group (gs % 64 == 0)
+        w_lo = __ldg(reinterpret_cast<const float4*>(w + k1 + 8 * c));
+        w_hi = __ldg(reinterpret_cast<const float4*>(w + k1 + 8 * c + 4));
+#pragma unroll
+        for (int i = 0; i < kBM / 32; ++i) nfv[i] = __ldg(p.nf + (m0 + rq + 32 * i) * p.G + g1);
+      }
 #pragma unroll
       for (int i = 0; i < kBM / 32; ++i) {
         const int r = rq + 32 * i;
-        const float nf = __ldg(p.nf + (m0 + r) * p.G + g);
+        const float nf = nfc[i];
         uint4 yv, gv;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(yv.x), "=r"(yv.y), "=r"(yv.z), "=r"(yv.w)
