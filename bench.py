@@ -188,15 +188,31 @@ def hbm_peak() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources that define the kernels and how a call launches
-    them (the host pipeline, ggrn_host.cu, only sequences copies around
-    those launches and is left out)."""
+    """Hash of the sources that define the norm kernels and how a call
+    launches them (the host pipeline, ggrn_host.cu, only sequences copies
+    around those launches, and ggrn_outproj.cu holds the separate fused
+    out_proj kernels: both are left out)."""
     h = hashlib.sha256()
     for fn in sorted(os.listdir(CSRC)):
-        if fn.endswith((".cu", ".cuh", ".h")) and fn != "ggrn_host.cu":
+        if fn.endswith((".cu", ".cuh", ".h")) and fn not in ("ggrn_host.cu", "ggrn_outproj.cu"):
             with open(os.path.join(CSRC, fn), "rb") as fh:
-                h.update(fn.encode() + b"\0" + fh.read())
+                h.update(fn.encode() + b"\0" + _without_timeline(fh.read()))
     return h.hexdigest()[:16]
+
+
+def _without_timeline(src: bytes) -> bytes:
+    """The source as the product library compiles it: the blocks compiled
+    only into the profiling build (#ifdef GGRN_TIMELINE ... #endif, not
+    nested) are dropped."""
+    out, skip = [], False
+    for line in src.split(b"\n"):
+        if line.strip() == b"#ifdef GGRN_TIMELINE":
+            skip = True
+        elif skip and line.strip() == b"#endif":
+            skip = False
+        elif not skip:
+            out.append(line)
+    return b"\n".join(out)
 
 
 def recorded_traffic(workload: str) -> tuple[float | None, str]:

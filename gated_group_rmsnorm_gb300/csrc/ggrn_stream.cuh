@@ -530,6 +530,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
   const int nvec = static_cast<int>(Q * gs / SE);
   const int vb = static_cast<int>(gs / SE);
   const int items_per_pass = W * TPW;
+#ifdef GGRN_TIMELINE
+  unsigned long long tl_first = 0;  // kept in registers: no global access in the loop
+  unsigned long long tl_units = 0;
+#endif
   // stage s of the ring and the parity of its current fill
   for (int s = 0, phase = 0;; s = (s + 1 == NS) ? 0 : s + 1, phase ^= (s == 0)) {
     if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(phase))) {
@@ -538,9 +542,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     }
     const int64_t u = c.unit_of[s];
 #ifdef GGRN_TIMELINE
-    if (warp == 0 && lane == 0 && GGRN_TIMELINE_ON && u >= 0) {
-      if (GGRN_TIMELINE_AT(p, 4) == 0) GGRN_TIMELINE_AT(p, 2) = timeline_now();
-      GGRN_TIMELINE_AT(p, 4) += 1;
+    if (u >= 0) {
+      if (tl_units == 0) tl_first = timeline_now();
+      ++tl_units;
     }
 #endif
     if (u < 0) break;
@@ -649,7 +653,13 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
 #ifdef GGRN_TIMELINE
-  if (lane == 0 && GGRN_TIMELINE_ON) atomicMax(&GGRN_TIMELINE_AT(p, 3), timeline_now());
+  if (lane == 0 && GGRN_TIMELINE_ON) {
+    atomicMax(&GGRN_TIMELINE_AT(p, 3), timeline_now());
+    if (warp == 0) {
+      GGRN_TIMELINE_AT(p, 2) = tl_first;
+      GGRN_TIMELINE_AT(p, 4) = tl_units;
+    }
+  }
 #endif
 }
 
