@@ -92,8 +92,12 @@ def _run(wl, d_model, rows_sample, packed=False, seed=0):
 
 
 def test_small_shapes():
+    # one tile per row block (no cluster), two (a pair of CTAs shares each A
+    # block) and four or more (clusters of four)
     for rows, width, gs, d_model in ((128, 256, 64, 64), (256, 1024, 256, 512),
-                                     (384, 960 * 2, 960, 480), (128, 640, 128, 96)):
+                                     (384, 960 * 2, 960, 480), (128, 640, 128, 96),
+                                     (256, 1024, 256, 1024), (128, 1920, 960, 1920),
+                                     (256, 512, 64, 4096)):
         wl = ggrn_inputs.Workload("op", rows, width, gs, torch.bfloat16, 0, 1e-5, sat_frac=0.01)
         _run(wl, d_model, list(range(rows)))
 
