@@ -25,6 +25,13 @@
 //             two accumulators in tensor memory; after the last block warps
 //             2-9 read the accumulators (tcgen05.ld), round to bf16 and store
 //             Z.  Two stages of shared memory; every wait is bounded.
+//
+// Each CTA of a row block rebuilds the same A block.  Sharing it across a
+// cluster of CTAs (each building a slice and storing it into every CTA's
+// shared memory, the stage released by a multicast commit) was correct but
+// slower: 4096 x 3840 x 7680 in 329 us with single CTAs, 599 with pairs, 716
+// with clusters of four -- every K block then waits for the slowest CTA of
+// the cluster and the remote arrivals, which two stages cannot hide.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -171,71 +178,11 @@ __global__ void __launch_bounds__(256) k_nf(const __nv_bfloat16* y, const __nv_b
 }
 
 // ---------------------------------------------------------------------------
-// Cluster helpers (CN > 1: the CTAs of a cluster share each A block).
+// k_outproj
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The address of the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   bar_cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
-      "%3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kWaitHintNs)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait that acquires at cluster scope (arrivals from other CTAs).
-__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (try_wait_cluster(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Arrive once on `bar` in every CTA of `mask` when this thread's MMAs are done.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// k_outproj<CN>: CN CTAs of a cluster (consecutive N tiles of one row block)
-// share each A block: CTA `rank` builds rows [rank*128/CN, (rank+1)*128/CN)
-// of it and stores them into every CTA's shared memory, so each element of A
-// is built d_model / (2 BNH CN) times instead of d_model / (2 BNH).
-// ---------------------------------------------------------------------------
-template <int CN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_outproj(const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_g,
               const __grid_constant__ CUtensorMap tm_b, const Params p) {
-  constexpr int kRowsOwn = kBM / CN;                        // A rows this CTA builds
-  constexpr int kRpt = kRowsOwn * 8 / kProducerThreads;     // 16-byte chunks per thread per block
-  static_assert(kRpt >= 1 && kRowsOwn % 32 == 0, "cluster size");
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte aligned base (the swizzled tiles need it)
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -243,18 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* base = smem_raw + (base_u - raw_u);
   const uint32_t bar_u = base_u + kStages * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
-  // barriers: full_yg[2] (this CTA's y and gate rows landed), yg_free[2]
-  // (this CTA's producers are done reading them), full_b[2] (W_out landed),
-  // full_a[2] (every CTA of the cluster stored its rows of the A block),
-  // stage_free[2] (every CTA's MMAs of the stage done: A and B free),
-  // acc_full; then the TMEM address slot and the abort flag
+  // barriers: full_yg[2] (y and gate landed), full_b[2] (W_out landed),
+  // full_a[2] (A built; also: y and gate read), empty_b[2] (the MMAs of the
+  // stage done: A and B free), acc_full; then the TMEM address slot and the
+  // abort flag
   auto full_yg = [&](int s) { return bar_u + 8u * s; };
-  auto yg_free = [&](int s) { return bar_u + 8u * (2 + s); };
-  auto full_b = [&](int s) { return bar_u + 8u * (4 + s); };
-  auto full_a = [&](int s) { return bar_u + 8u * (6 + s); };
-  auto stage_free = [&](int s) { return bar_u + 8u * (8 + s); };
-  const uint32_t acc_full = bar_u + 8u * 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  auto full_b = [&](int s) { return bar_u + 8u * (2 + s); };
+  auto full_a = [&](int s) { return bar_u + 8u * (4 + s); };
+  auto empty_b = [&](int s) { return bar_u + 8u * (6 + s); };
+  const uint32_t acc_full = bar_u + 8u * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   auto sA = [&](int s) { return base_u + s * kStageBytes; };
   auto sB = [&](int s) { return base_u + s * kStageBytes + kABytes; };
@@ -263,20 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bnh = p.bnh;
-  const uint32_t rank = CN > 1 ? cluster_rank() : 0u;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kBM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 2 * bnh;
   const int KB = static_cast<int>(p.K / kBK);
   const uint32_t b_half_bytes = static_cast<uint32_t>(bnh) * kBK * 2;
-  const uint32_t own_bytes = kRowsOwn * kBK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_yg(s), 1);
-      mbar_init(yg_free(s), kProducerThreads / 32);
       mbar_init(full_b(s), 1);
-      mbar_init(full_a(s), CN * kProducerThreads / 32);
-      mbar_init(stage_free(s), CN);
+      mbar_init(full_a(s), kProducerThreads);
+      mbar_init(empty_b(s), 1);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -285,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
-  if constexpr (CN > 1) cluster_sync();  // every CTA's barriers exist before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // nothing global is read before the previous kernel (the nf pass) is done
@@ -293,16 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
 
   if (warp == 0) {
-    // ---- copies: lane 0 this CTA's rows of y and gate (refilled once its
-    // producers have read them), lane 1 the two W_out halves (refilled once
-    // every CTA's MMAs of the stage are done) ----
+    // ---- copies: lane 0 y and gate (refilled once the A block is built
+    // from them), lane 1 the two W_out halves (refilled once the stage's
+    // MMAs are done) ----
     if (lane < 2) {
       const bool yg = lane == 0;
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
         const uint32_t prev = static_cast<uint32_t>(kb / kStages - 1) & 1u;
-        if (kb >= kStages && !(yg ? mbar_wait(yg_free(s), prev) : wait_cluster(stage_free(s), prev))) {
+        if (kb >= kStages && !mbar_wait(yg ? full_a(s) : empty_b(s), prev)) {
           *abort_flag = 1;
           atomicOr(p.fault, kFaultGemmWait);
           break;
@@ -310,10 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag) break;
         const int k0 = kb * kBK;
         if (yg) {
-          const int row = static_cast<int>(m0 + rank * kRowsOwn);
-          mbar_expect_tx(full_yg(s), 2 * own_bytes);
-          tma_load_2d(sY(s), &tm_y, k0, row, full_yg(s));
-          tma_load_2d(sG(s), &tm_g, k0, row, full_yg(s));
+          mbar_expect_tx(full_yg(s), 2 * kYBytes);
+          tma_load_2d(sY(s), &tm_y, k0, static_cast<int>(m0), full_yg(s));
+          tma_load_2d(sG(s), &tm_g, k0, static_cast<int>(m0), full_yg(s));
         } else {
           mbar_expect_tx(full_b(s), 2 * b_half_bytes);
           tma_load_2d(sB(s), &tm_b, k0, static_cast<int>(n0), full_b(s));
@@ -334,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-        if (*abort_flag || !wait_cluster(full_a(s), ph) || !mbar_wait(full_b(s), ph)) {
+        if (*abort_flag || !mbar_wait(full_a(s), ph) || !mbar_wait(full_b(s), ph)) {
           *abort_flag = 1;
           atomicOr(p.fault, kFaultGemmWait);
           break;
@@ -350,106 +290,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem, a_desc + adv, b_desc0 + adv, idesc, kb > 0 || kk > 0);
           mma_bf16(tmem + kHalfCol, a_desc + adv, b_desc1 + adv, idesc, kb > 0 || kk > 0);
         }
-        // the stage is free once these MMAs have read it: in every CTA of the
-        // cluster, whose producers also write this CTA's A block
-        if constexpr (CN > 1)
-          mma_commit_multicast(stage_free(s), static_cast<uint16_t>((1u << CN) - 1u));
-        else
-          mma_commit(stage_free(s));
+        mma_commit(empty_b(s));  // frees A and B of the stage once these MMAs have read them
       }
       mma_commit(acc_full);  // the accumulators are complete (or abandoned)
       // wait for it here too, so that no MMA still runs when TMEM is freed
       if (!mbar_wait(acc_full, 0)) atomicOr(p.fault, kFaultGemmWait);
     }
   } else {
-    // ---- A blocks: warps 2-9 build this CTA's kRowsOwn rows ----
+    // ---- A blocks: warps 2-9 ----
     const int t = threadIdx.x - 64;       // 0..255
-    const int rq = t >> 3;                // row (within 32) of this thread's first chunk
+    const int rq = t >> 3;                // row within a group of 32 rows
     const int c = t & 7;                  // 16-byte chunk (8 columns) of the 64
     const float* w = p.w;
-    // the rows' A block addresses in every CTA of the cluster
-    uint32_t peer_delta[CN];
-#pragma unroll
-    for (int q = 0; q < CN; ++q) peer_delta[q] = CN > 1 ? map_to(base_u, q) - base_u : 0u;
     // the weight columns and normalisers of the next block are fetched one
     // block ahead (their global-memory latency then overlaps this block)
     float4 w_lo = __ldg(reinterpret_cast<const float4*>(w + 8 * c));
     float4 w_hi = __ldg(reinterpret_cast<const float4*>(w + 8 * c + 4));
-    float nfv[kRpt];
+    float nfv[kBM / 32];
 #pragma unroll
-    for (int i = 0; i < kRpt; ++i)
-      nfv[i] = __ldg(p.nf + (m0 + rank * kRowsOwn + rq + 32 * i) * p.G);
+    for (int i = 0; i < kBM / 32; ++i) nfv[i] = __ldg(p.nf + (m0 + rq + 32 * i) * p.G);
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % kStages;
       const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-      // this CTA's y and gate rows landed; every CTA's A[s] free (the MMAs
-      // of kb - 2 done everywhere)
+      // y and gate of this block landed; A[s] free (the MMAs of kb - 2 done)
       if (*abort_flag || !mbar_wait(full_yg(s), ph) ||
-          (kb >= kStages && !wait_cluster(stage_free(s), ph ^ 1u))) {
+          (kb >= kStages && !mbar_wait(empty_b(s), ph ^ 1u))) {
         *abort_flag = 1;
         if (lane == 0) atomicOr(p.fault, kFaultGemmWait);
         break;
       }
       const int64_t k0 = static_cast<int64_t>(kb) * kBK;
       const float wv[8] = {w_lo.x, w_lo.y, w_lo.z, w_lo.w, w_hi.x, w_hi.y, w_hi.z, w_hi.w};
-      float nfc[kRpt];
+      float nfc[kBM / 32];
 #pragma unroll
-      for (int i = 0; i < kRpt; ++i) nfc[i] = nfv[i];
+      for (int i = 0; i < kBM / 32; ++i) nfc[i] = nfv[i];
       if (kb + 1 < KB) {
         const int64_t k1 = k0 + kBK;
         const int64_t g1 = k1 / p.gs;  // a K block never crosses a group (gs % 64 == 0)
         w_lo = __ldg(reinterpret_cast<const float4*>(w + k1 + 8 * c));
         w_hi = __ldg(reinterpret_cast<const float4*>(w + k1 + 8 * c + 4));
 #pragma unroll
-        for (int i = 0; i < kRpt; ++i)
-          nfv[i] = __ldg(p.nf + (m0 + rank * kRowsOwn + rq + 32 * i) * p.G + g1);
+        for (int i = 0; i < kBM / 32; ++i) nfv[i] = __ldg(p.nf + (m0 + rq + 32 * i) * p.G + g1);
       }
 #pragma unroll
-      for (int i = 0; i < kRpt; ++i) {
-        const int rl = rq + 32 * i;                         // row within this CTA's rows
-        const int r = static_cast<int>(rank) * kRowsOwn + rl;  // row within the A block
+      for (int i = 0; i < kBM / 32; ++i) {
+        const int r = rq + 32 * i;
+        const float nf = nfc[i];
         uint4 yv, gv;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(yv.x), "=r"(yv.y), "=r"(yv.z), "=r"(yv.w)
-                     : "r"(sY(s) + rl * 128 + c * 16));
+                     : "r"(sY(s) + r * 128 + c * 16));
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(gv.x), "=r"(gv.y), "=r"(gv.z), "=r"(gv.w)
-                     : "r"(sG(s) + rl * 128 + c * 16));
+                     : "r"(sG(s) + r * 128 + c * 16));
         float yf[8], gf[8], a[8], o[8];
         Elem<__nv_bfloat16>::unpack(yv, yf);
         Elem<__nv_bfloat16>::unpack(gv, gf);
         gated_vec<__nv_bfloat16, 8>(yf, gf, a);
-        mamba2_out<__nv_bfloat16, 8>(a, nfc[i], nfc[i], wv, o);
+        mamba2_out<__nv_bfloat16, 8>(a, nf, nf, wv, o);
         const uint4 av = Elem<__nv_bfloat16>::pack(o);
         // the 128-byte swizzle: chunk c of row r at chunk c ^ (r mod 8)
         const uint32_t dst = sA(s) + r * 128 + ((c ^ (r & 7)) << 4);
-        if constexpr (CN > 1) {
-#pragma unroll
-          for (int q = 0; q < CN; ++q) st_cluster_v4(dst + peer_delta[q], av);
-        } else {
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(av.x),
-                       "r"(av.y), "r"(av.z), "r"(av.w)
-                       : "memory");
-        }
-        if (p.a_out && blockIdx.x < CN)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(av.x), "r"(av.y),
+                     "r"(av.z), "r"(av.w)
+                     : "memory");
+        if (p.a_out && blockIdx.x == 0)
           *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.a_out) + (m0 + r) * p.K + k0 +
                                     8 * c) = av;
       }
-      // the tensor cores read the block through the async proxy
-      if constexpr (CN > 1)
-        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-      else
-        fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(yg_free(s));
-        if constexpr (CN > 1) {
-#pragma unroll
-          for (int q = 0; q < CN; ++q) arrive_cluster(map_to(full_a(s), q));
-        } else {
-          mbar_arrive(full_a(s));
-        }
-      }
+      fence_async_smem();  // the tensor cores read the block through the async proxy
+      mbar_arrive(full_a(s));
     }
     // ---- epilogue: accumulators -> bf16 Z ----
     const bool ok = mbar_wait(acc_full, 0) && !*abort_flag;
@@ -482,9 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while another can still write its shared memory or arrive
-  // on its barriers
-  if constexpr (CN > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -546,40 +453,6 @@ bool ranges_overlap_bytes(const void* a, int64_t na, const void* b, int64_t nb) 
   if (na <= 0 || nb <= 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
   return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
-}
-
-// Largest cluster of CTAs sharing an A block.
-constexpr int kMaxCluster = 4;
-
-template <int CN>
-cudaError_t launch_outproj(const CUtensorMap& tm_y, const CUtensorMap& tm_g,
-                           const CUtensorMap& tm_b, const Params& p, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_outproj<CN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kSmemBytes));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.N / (2 * p.bnh)), static_cast<unsigned>(p.M / kBM));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  int n = 1;
-  if (CN > 1) {
-    at[1].id = cudaLaunchAttributeClusterDimension;
-    at[1].val.clusterDim.x = CN;
-    at[1].val.clusterDim.y = 1;
-    at[1].val.clusterDim.z = 1;
-    n = 2;
-  }
-  cfg.attrs = at;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, k_outproj<CN>, tm_y, tm_g, tm_b, p);
 }
 
 }  // namespace outproj
@@ -650,13 +523,9 @@ extern "C" int ggrn_norm_outproj(const void* y, const void* gate, const void* w,
   const int64_t G = width / group_size;
   unsigned int* fault = device_fault_word();
   if (!fault) return GGRN_ERR_CUDA;
-  // CTAs per cluster sharing each A block: the most (of 4, 2, 1) that
-  // divides the N tiles of a row block
-  const int64_t n_tiles = d_model / (2 * bnh);
-  const int cn = n_tiles % kMaxCluster == 0 ? kMaxCluster : (n_tiles % 2 == 0 ? 2 : 1);
   CUtensorMap tm_y, tm_g, tm_b;
-  if (!make_map(&tm_y, y, width, rows, ys, kBK, static_cast<uint32_t>(kBM / cn), false) ||
-      !make_map(&tm_g, gate, width, rows, gts, kBK, static_cast<uint32_t>(kBM / cn), false) ||
+  if (!make_map(&tm_y, y, width, rows, ys, kBK, kBM, false) ||
+      !make_map(&tm_g, gate, width, rows, gts, kBK, kBM, false) ||
       !make_map(&tm_b, w_out, width, d_model, width, kBK, static_cast<uint32_t>(bnh), true))
     return GGRN_ERR_UNSUPPORTED;
   const cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -684,6 +553,16 @@ extern "C" int ggrn_norm_outproj(const void* y, const void* gate, const void* w,
   }
   // the GEMM
   {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(k_outproj, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmemBytes));
+    });
+    if (attr_err != cudaSuccess) {
+      record_cuda_error(attr_err);
+      return GGRN_ERR_CUDA;
+    }
     Params p;
     p.w = static_cast<const float*>(w);
     p.nf = nf;
@@ -696,12 +575,17 @@ extern "C" int ggrn_norm_outproj(const void* y, const void* gate, const void* w,
     p.gs = group_size;
     p.G = G;
     p.bnh = bnh;
-    cudaError_t e;
-    switch (cn) {
-      case 4: e = launch_outproj<4>(tm_y, tm_g, tm_b, p, s); break;
-      case 2: e = launch_outproj<2>(tm_y, tm_g, tm_b, p, s); break;
-      default: e = launch_outproj<1>(tm_y, tm_g, tm_b, p, s); break;
-    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d_model / (2 * bnh)), static_cast<unsigned>(rows / kBM));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_outproj, tm_y, tm_g, tm_b, p);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       return GGRN_ERR_CUDA;
