@@ -307,11 +307,27 @@ def _decode_numbers(g, device) -> dict:
     g21_dev, g21_wall = timed(lambda: g21.replay(stream), n_calls // 21)
     g1.close()
     g21.close()
+    # the same step of a norm whose row is one 7680-wide group (a cluster of
+    # CTAs per group): 21 calls in one graph
+    lone = []
+    for i in range(21):
+        inp = ggrn_inputs.random_case(1, 7680, 7680, torch.bfloat16, 0, seed=300 + i)
+        lone.append((inp.y.to(device), inp.gate.to(device), inp.w.to(device),
+                     torch.empty((1, 7680), dtype=torch.bfloat16, device=device)))
+    plan_lone = g.plan(lone[0][0], lone[0][1], lone[0][2], group_size=7680)
+    gl = g.DecodeGraph([dict(y=y, gate=gt, w=w, out=o, group_size=7680, eps=1e-5)
+                        for y, gt, w, o in lone])
+    gl_dev, gl_wall = timed(lambda: gl.replay(stream), n_calls // 21)
+    gl.close()
     return {"workload": "mamba2_decode (1 x 7680, groups of 960, bf16)",
             "eager_us_per_call": round(max(dev_us, wall_us) / n_calls, 3),
             "graph1_us_per_call": round(max(g1_dev, g1_wall) / n_calls, 3),
             "graph21_us_per_call": round(max(g21_dev, g21_wall) / (21 * (n_calls // 21)), 3),
-            "note": "max(device time, host wall time) per call over back-to-back calls"}
+            "lone_group_7680_graph21_us_per_call":
+                round(max(gl_dev, gl_wall) / (21 * (n_calls // 21)), 3),
+            "lone_group_path": plan_lone["path_name"],
+            "note": "max(device time, host wall time) per call over back-to-back calls; "
+                    "DecodeGraph is for chains (a 1-call graph costs more than the eager call)"}
 
 
 def _outproj_numbers(g, device, steps: int, d_models=(3840, 7680)) -> dict:

@@ -11,7 +11,8 @@ computed by hand-written CUDA kernels behind a C ABI (``include/ggrn.h``,
 ``libggrn.so``).  This package is the thin Python binding.
 """
 from .binding import (BF16, DTYPE_CODE, F16, F32, MAMBA2, ONNX, PATH_AUTO, PATH_NAMES,
-                      PATH_SCALAR, PATH_STRADDLE, PATH_STREAM, PATH_TEAM, PATH_WIDE, DecodeGraph,
+                      PATH_SCALAR, PATH_STRADDLE, PATH_STREAM, PATH_TEAM, PATH_WIDE,
+                      PATH_WIDE_CLUSTER, DecodeGraph,
                       GgrnError, fault_status, forward, forward_host, forward_inproj,
                       ggrn_forward, ggrn_forward_host, ggrn_forward_inproj,
                       ggrn_forward_inproj_host, ggrn_forward_noalloc, ggrn_forward_path,
@@ -23,4 +24,4 @@ __all__ = ["forward", "forward_host", "forward_inproj", "plan", "DecodeGraph", "
            "ggrn_forward_noalloc", "ggrn_norm_outproj", "norm_outproj",
            "ggrn_forward_path", "ggrn_plan", "host_workspace", "load",
            "library_path", "status_string", "MAMBA2", "ONNX", "F32", "F16", "BF16", "PATH_AUTO", "PATH_TEAM", "PATH_WIDE", "PATH_STRADDLE", "PATH_SCALAR",
-           "PATH_STREAM", "PATH_NAMES", "DTYPE_CODE", "fault_status"]
+           "PATH_STREAM", "PATH_WIDE_CLUSTER", "PATH_NAMES", "DTYPE_CODE", "fault_status"]

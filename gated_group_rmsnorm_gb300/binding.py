@@ -21,9 +21,11 @@ from . import build as _build
 # ggrn_dtype / ggrn_mode / ggrn_path
 F32, F16, BF16 = 0, 1, 2
 MAMBA2, ONNX = 0, 1
-PATH_AUTO, PATH_TEAM, PATH_WIDE, PATH_STRADDLE, PATH_SCALAR, PATH_STREAM = range(6)
+PATH_AUTO, PATH_TEAM, PATH_WIDE, PATH_STRADDLE, PATH_SCALAR, PATH_STREAM, PATH_WIDE_CLUSTER = \
+    range(7)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_TEAM: "team", PATH_WIDE: "wide",
-              PATH_STRADDLE: "straddle", PATH_SCALAR: "scalar", PATH_STREAM: "stream"}
+              PATH_STRADDLE: "straddle", PATH_SCALAR: "scalar", PATH_STREAM: "stream",
+              PATH_WIDE_CLUSTER: "wide_cluster"}
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 MODE_CODE = {"mamba2": MAMBA2, "onnx": ONNX, MAMBA2: MAMBA2, ONNX: ONNX}
 

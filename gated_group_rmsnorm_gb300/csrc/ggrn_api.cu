@@ -115,6 +115,9 @@ constexpr int kTeamBlock = 256;
 constexpr int kTeamMaxVec = 128;     // TEAM covers groups of up to 128 vectors
 constexpr int kWideVpl = 4;
 constexpr int kWideMaxThreads = 1024;
+// automatic selection takes WIDE_CLUSTER for groups of at least this many
+// 16-byte vectors when every CTA of every cluster fits on the GPU at once
+constexpr int64_t kWideClusterAutoVecs = 256;
 constexpr int kStraddleMaxVpl = 4;   // chunk of at most 128 vectors per warp
 constexpr int kStraddleBlock = 256;
 constexpr int kScalarBlock = 256;
@@ -314,6 +317,41 @@ int wide_vpl(const Args& a, int64_t items, int64_t sms) {
   if (v == 1 && nvec > kWideOneVecMaxThreads) v = 2;
   while (v < 4 && ceil_div(nvec, v) > kWideMaxThreads) v *= 2;
   return v;
+}
+
+// WIDE_CLUSTER: a cluster of CTAs per group, one 16-byte vector per thread;
+// up to kWideClusterMax CTAs of about kWideClusterVecs vectors each.
+// (Measured on lone 2048..7680-wide bf16 groups: 2 or 4 CTAs of 256..512
+// threads, and 16-CTA clusters of 64 or 96 threads, were no faster.)
+constexpr int kWideClusterMax = 8;     // the portable cluster size
+constexpr int kWideClusterVecs = 128;  // vectors per CTA sought
+int plan_wide_cluster(const Args& a, Plan* p) {
+  const int es = elem_size(a.dtype);
+  const int E = 16 / es;
+  if (a.gs % E != 0) return GGRN_ERR_UNSUPPORTED;
+  const int64_t nvec = a.gs / E;
+  if (nvec < 2) return GGRN_ERR_UNSUPPORTED;
+  const int64_t cn = std::max<int64_t>(
+      2, std::min<int64_t>(kWideClusterMax, ceil_div(nvec, kWideClusterVecs)));
+  const int64_t per = ceil_div(nvec, cn);
+  const int64_t threads = ceil_div(per, 32) * 32;
+  // the kernel has 32 slots: one per warp of the cluster
+  if (cn * (threads / 32) > 32) return GGRN_ERR_UNSUPPORTED;
+  p->path = kWideCluster;
+  p->elems_per_vec = E;
+  p->nvec = static_cast<int>(nvec);
+  p->vpl = 1;
+  p->lanes = static_cast<int>(threads);
+  p->block = static_cast<int>(threads);
+  p->cluster_ctas = static_cast<int>(cn);
+  p->cluster_vecs = static_cast<int>(per);
+  p->groups = a.width / a.gs;
+  p->items = a.rows * p->groups;
+  p->div_magic = div_magic(p->items, p->groups);
+  if (p->items > kMaxGrid / cn) return GGRN_ERR_UNSUPPORTED;
+  p->grid = p->items * cn;
+  p->smem = 0;
+  return GGRN_OK;
 }
 
 int plan_straddle(const Args& a, Plan* p) {
@@ -614,6 +652,14 @@ int make_plan(const Args& a, int path, Plan* p) {
         // of 30 elements per lane).
         const int64_t items = a.rows * (a.width / a.gs);
         const int64_t sms = sm_count();
+        // A few wide groups (a batch-1 step of a norm with one wide group):
+        // a cluster of CTAs per group, the partial sums of squares combined
+        // through distributed shared memory, so each CTA's chain of loads
+        // is short.
+        if (a.gs / (16 / elem_size(a.dtype)) >= kWideClusterAutoVecs &&
+            plan_wide_cluster(a, p) == GGRN_OK && p->grid <= sms)
+          return GGRN_OK;
+        *p = Plan();
         if (items <= sms) {
           if (plan_wide(a, p, wide_vpl(a, items, sms)) == GGRN_OK) return GGRN_OK;
           *p = Plan();
@@ -638,6 +684,9 @@ int make_plan(const Args& a, int path, Plan* p) {
     case kStream:
       if (!vec_ok) return GGRN_ERR_ALIGN;
       return plan_stream(a, p, true);
+    case kWideCluster:
+      if (!vec_ok) return GGRN_ERR_ALIGN;
+      return plan_wide_cluster(a, p);
     default:
       return GGRN_ERR_ARG;
   }
@@ -820,6 +869,8 @@ KParams make_params(const Args& a, const Plan& p) {
   k.head_units = p.head_units;
   k.head_size = p.head_size;
   k.team_map = p.team_map;
+  k.cluster_ctas = p.cluster_ctas;
+  k.cluster_vecs = p.cluster_vecs;
   k.rows = a.rows;
   k.fault = nullptr;
   k.no_copies = 0;
@@ -849,7 +900,7 @@ extern "C" int ggrn_forward_path(const void* y, const void* gate, const void* w,
                                  int64_t y_row_stride, int64_t gate_row_stride,
                                  int64_t out_row_stride, float eps, int dtype, int mode,
                                  int path, void* cuda_stream) {
-  if (path < kAuto || path > kStream) return GGRN_ERR_ARG;
+  if (path < kAuto || path > kWideCluster) return GGRN_ERR_ARG;
   const Args a = make_args(y, gate, w, out, rows, width, group_size, y_row_stride,
                            gate_row_stride, out_row_stride, eps, dtype, mode);
   return forward_impl(a, path, static_cast<cudaStream_t>(cuda_stream));
@@ -880,7 +931,7 @@ extern "C" int ggrn_plan(const void* y, const void* gate, const void* w, const v
                          int64_t gate_row_stride, int64_t out_row_stride, int dtype, int mode,
                          int path, ggrn_plan_info* info) {
   if (!info) return GGRN_ERR_ARG;
-  if (path < kAuto || path > kStream) return GGRN_ERR_ARG;
+  if (path < kAuto || path > kWideCluster) return GGRN_ERR_ARG;
   std::memset(info, 0, sizeof(*info));
   const Args a = make_args(y, gate, w, const_cast<void*>(out), rows, width, group_size,
                            y_row_stride, gate_row_stride, out_row_stride, 0.0f, dtype, mode);

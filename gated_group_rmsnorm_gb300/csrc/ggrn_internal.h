@@ -9,7 +9,9 @@ namespace ggrn {
 
 enum Mode : int { kMamba2 = 0, kOnnx = 1 };
 enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
-enum Path : int { kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4, kStream = 5 };
+enum Path : int {
+  kAuto = 0, kTeam = 1, kWide = 2, kStraddle = 3, kScalar = 4, kStream = 5, kWideCluster = 6
+};
 // STREAM with 8 teams per warp: how the teams of a warp's pass take its 8
 // consecutive items (see plan_stream)
 enum TeamMap : int { kTeamsInOrder = 0, kTeamsApart2 = 1, kTeamsApart4 = 2 };
@@ -65,6 +67,9 @@ struct Plan {
   int team_map = kTeamsInOrder;
   uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
   int ctas_per_sm = 0;
+  // WIDE_CLUSTER: CTAs per group (the cluster) and vectors per CTA
+  int cluster_ctas = 0;
+  int cluster_vecs = 0;
 };
 
 // Most consumer warps of a streaming launch (the kernels' launch bounds).
@@ -121,6 +126,8 @@ struct KParams {
   int no_copies;              // STREAM self-test: the producer issues nothing
   unsigned long long* sched;  // STREAM: unit-claim word, or NULL (static schedule)
   uint32_t epoch;             // STREAM: this launch's claim epoch (nonzero)
+  int cluster_ctas;            // WIDE_CLUSTER: CTAs per group
+  int cluster_vecs;            // WIDE_CLUSTER: vectors per CTA
   float eps;
   float gs_f;
 };

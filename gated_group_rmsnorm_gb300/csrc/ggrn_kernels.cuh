@@ -827,6 +827,116 @@ __global__ void __launch_bounds__(256) k_scalar(const KParams p) {
 // Launch of the kernel a plan names, for one element type.
 // ---------------------------------------------------------------------------
 // The streaming family lives in ggrn_stream.cuh.
+// ---------------------------------------------------------------------------
+// k_wide_cluster: one cluster of CN CTAs per group (a few wide groups: a
+// batch-1 decode step of a norm with one wide group).  CTA `rank` takes
+// vectors [rank * per, (rank + 1) * per) of the group, one per thread
+// (per = p.cluster_vecs; CTAs x warps per CTA <= 32).  Lane r of each warp
+// stores the warp's partial sum of squares into slot rank * warps + warp of
+// CTA r's shared memory (distributed shared memory); after one cluster
+// barrier every warp of every CTA adds the 32 slots with the same butterfly,
+// so all CTAs get the same bits and no CTA touches another after the
+// barrier.  A relaxed cluster arrive at entry, waited on just before the
+// first remote store, makes sure every CTA of the cluster is running before
+// its shared memory is written.  Cluster barriers are hardware barriers over
+// co-scheduled CTAs: every CTA reaches each of them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store v at the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f32(float* own_addr, uint32_t rank, float v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(own_addr));
+  uint32_t m;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(m), "f"(v) : "memory");
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(512) k_wide_cluster(const KParams p) {
+  constexpr int E = Elem<T>::E;
+  // slot r * nwarps + w: warp w of CTA r's partial sum (CTAs x warps <= 32)
+  __shared__ float partials[32];
+  cluster_arrive_relaxed();  // this CTA is running (waited on before the pushes)
+  pdl_wait();
+  pdl_launch_dependents();
+  const int CN = p.cluster_ctas;  // CTAs per cluster (the launch's cluster size)
+  const uint32_t rank = cluster_ctarank();
+  const int64_t item = blockIdx.x / CN;  // the group of this cluster
+  const int tid = threadIdx.x;
+  const int nwarps = blockDim.x >> 5;
+  const int64_t row = div_by(item, p.groups, p.div_magic);
+  const int64_t g = item - row * p.groups;
+  const int64_t col0 = g * p.gs;
+  const int v = static_cast<int>(rank) * p.cluster_vecs + tid;  // this thread's vector
+  const bool has = tid < p.cluster_vecs && v < p.nvec;
+  const T* yp = static_cast<const T*>(p.y) + row * p.ys + col0;
+  const T* gp = static_cast<const T*>(p.gate) + row * p.gts + col0;
+  uint4 yr = make_uint4(0u, 0u, 0u, 0u), gr = make_uint4(0u, 0u, 0u, 0u);
+  float wv[E];
+  if (has) {
+    yr = ld_stream(yp + (int64_t)v * E);
+    gr = ld_stream(gp + (int64_t)v * E);
+    load_weight_vec<T, MODE>(p.w, (MODE == kMamba2 ? col0 : 0) + (int64_t)v * E, wv);
+  }
+  float a[E];
+  float c0 = 0.0f, c1 = 0.0f;
+  {
+    float yf[E];
+    Elem<T>::unpack(yr, yf);
+    if (MODE == kMamba2) {
+      float gf[E];
+      Elem<T>::unpack(gr, gf);
+      gated_vec<T, E>(yf, gf, a);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[e] = yf[e];
+    }
+    sumsq2<E>(a, c0, c1);
+  }
+  float ss = c0 + c1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  // every warp pushes its partial to its slot in every CTA of the cluster
+  // (lane r stores to CTA r)
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nslots = CN * nwarps;
+  cluster_wait();  // every CTA of the cluster has started
+  if (lane < CN)
+    st_cluster_f32(&partials[static_cast<int>(rank) * nwarps + warp], static_cast<uint32_t>(lane), ss);
+  cluster_barrier();  // every warp's partial is in every CTA's slots
+  // a warp butterfly over the 32 slots (0 past the used ones): the same
+  // operations, hence the same bits, in every warp of every CTA
+  float m2 = lane < nslots ? partials[lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+  const float nf = normaliser(m2, p.gs_f, p.eps);
+  if (has) {
+    uint4 o;
+    if (MODE == kMamba2) {
+      o = epilogue_mamba2<T>(a, nf, wv);
+    } else {
+      float gf[E], sg[E];
+      Elem<T>::unpack(gr, gf);
+      silu_vec<T, E>(gf, sg);
+      o = epilogue_onnx<T>(a, sg, nf, wv);
+    }
+    st_stream(static_cast<T*>(p.out) + row * p.os + col0 + (int64_t)v * E, o);
+  }
+}
+
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s);
 
@@ -916,6 +1026,22 @@ cudaError_t launch_mode(const KParams& k, const Plan& p, cudaStream_t s) {
       break;
     case kStream:
       return launch_stream<T, MODE>(k, p, s);
+    case kWideCluster: {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+      cfg.blockDim = dim3(static_cast<unsigned>(p.block));
+      cfg.stream = s;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster_ctas);
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      return cudaLaunchKernelEx(&cfg, k_wide_cluster<T, MODE>, k);
+    }
     default:
       break;
   }

@@ -86,10 +86,15 @@ typedef enum {
   GGRN_PATH_SCALAR = 4,   /* element loads, any alignment and any group size; the group is
                              read twice (a correctness path for layouts the vector paths
                              cannot load) */
-  GGRN_PATH_STREAM = 5    /* persistent CTAs; a producer lane streams row chunks into a
+  GGRN_PATH_STREAM = 5,   /* persistent CTAs; a producer lane streams row chunks into a
                              shared-memory ring with bulk (TMA) copies, consumer warps
                              reduce from shared memory (group bytes a multiple of 8,
                              4..128 shared-memory vectors per group, enough rows) */
+  GGRN_PATH_WIDE_CLUSTER = 6 /* a cluster of 2..8 CTAs per group, one 16-byte vector per
+                                thread; the CTAs' partial sums of squares are combined
+                                through distributed shared memory (a few wide groups, e.g.
+                                a batch-1 step of a norm with one wide group; group a
+                                multiple of the vector, at most 1024 vectors) */
 } ggrn_path;
 
 /*

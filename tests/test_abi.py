@@ -185,8 +185,22 @@ def test_plan_selects_families():
     assert (p.path, p.elems_per_vec, p.team_lanes, p.vec_per_lane) == (g.PATH_TEAM, 4, 8, 4)
     p = _plan(8, 128, 128, 0)
     assert (p.path, p.elems_per_vec, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 4, 32, 1)
-    # a group too wide for registers goes to the scalar two-pass path
-    assert _plan(2, 1 << 16, 1 << 16, 2).path == g.PATH_SCALAR
+    # a few wide groups (256..1024 vectors): a cluster of up to 8 CTAs of up
+    # to 128 threads per group; the decode shape's 960-wide groups stay one
+    # CTA each
+    p = _plan(1, 7680, 7680, 2)
+    assert (p.path, p.block_threads, p.grid_blocks) == (g.PATH_WIDE_CLUSTER, 128, 8)
+    p = _plan(2, 8192, 8192, 2)
+    assert (p.path, p.block_threads, p.grid_blocks) == (g.PATH_WIDE_CLUSTER, 128, 16)
+    assert _plan(1, 5120, 5120, 2).path == g.PATH_WIDE_CLUSTER
+    assert _plan(2, 1 << 16, 1 << 16, 2).path == g.PATH_SCALAR   # beyond 1024 vectors
+    assert _plan(1, 7680, 960, 2).path == g.PATH_WIDE
+    assert _plan(1, 1024, 1024, 2).path == g.PATH_WIDE        # below 256 vectors
+    # too many groups for every cluster to be resident at once: the one-CTA path
+    assert _plan(64, 5120, 5120, 2).path != g.PATH_WIDE_CLUSTER
+    # a group too wide for registers even across a cluster goes to the
+    # scalar two-pass path
+    assert _plan(2, 1 << 17, 1 << 17, 2).path == g.PATH_SCALAR
     # rows == 0 still plans, with nothing to launch
     assert _plan(0, 7680, 960, 2).grid_blocks == 0
 
@@ -350,7 +364,7 @@ def test_plans_respect_launch_limits():
             continue
         rows = rnd.choice((1, 2, 7, 64, 1000, 4096, 20000, 70000))
         ys = width + rnd.choice((0, 0, 8, 64))
-        path = rnd.choice((0, 0, 1, 2, 3, 4, 5))
+        path = rnd.choice((0, 0, 1, 2, 3, 4, 5, 6))
         st, info = g.ggrn_plan(1 << 40, 2 << 40, 3 << 40, 0, rows, width, gs, ys, ys, width, dtype,
                                mode, path)
         if st != binding.OK:
@@ -365,7 +379,13 @@ def test_plans_respect_launch_limits():
             bound = 16 if info.vec_per_lane == 7 else 17   # consumer warps + producer
             assert info.block_threads <= bound * 32, case
             assert info.smem_bytes > 0, case
+        if info.path == g.PATH_WIDE_CLUSTER:
+            # whole clusters of 2..8 CTAs, one per group
+            ctas = info.grid_blocks // info.items
+            assert 2 <= ctas <= 8 and ctas * info.items == info.grid_blocks, case
         if path == 0:
             assert info.path in (g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR,
-                                 g.PATH_STREAM), case
+                                 g.PATH_STREAM, g.PATH_WIDE_CLUSTER), case
+            if info.path == g.PATH_WIDE_CLUSTER:
+                assert info.grid_blocks <= 152, case   # every cluster resident at once
     assert checked > 500

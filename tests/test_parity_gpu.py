@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 MAMBA2, ONNX = 0, 1
 WL = ggrn_inputs.WORKLOADS
-PATHS = (g.PATH_AUTO, g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR, g.PATH_STREAM)
+PATHS = (g.PATH_AUTO, g.PATH_TEAM, g.PATH_WIDE, g.PATH_STRADDLE, g.PATH_SCALAR, g.PATH_STREAM,
+         g.PATH_WIDE_CLUSTER)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -117,6 +118,28 @@ def test_sweep_every_path(dtype, mode):
     assert not failures, failures[:10]
     for p in PATHS:
         assert covered[p] > 0, f"path {g.PATH_NAMES[p]} never ran"
+
+
+@pytest.mark.parametrize("dtype,mode", list(_combos()),
+                         ids=lambda v: str(v).replace("torch.", ""))
+def test_lone_wide_groups(dtype, mode):
+    """A batch-1 step of a norm with one wide group (and a row of two):
+    automatic selection takes a cluster of CTAs per group (from 256 vectors);
+    every element against the oracle."""
+    cases = [(1, 7680, 7680), (1, 5120, 5120), (1, 2048, 2048), (1, 8200, 8200),
+             (2, 10240, 5120), (1, 8192, 8192)]
+    for rows, width, gs in cases:
+        inp = ggrn_inputs.random_case(rows, width, gs, dtype, mode, seed=width + rows,
+                                      std=1.5)
+        dev = gpu_util.to_device(inp)
+        wl = ggrn_inputs.Workload("lone", rows, width, gs, dtype, mode, 1e-5)
+        plan = g.plan(dev.y, dev.gate, dev.w, group_size=gs, mode=mode)
+        out = _run(dev, wl)
+        torch.cuda.synchronize()
+        gpu_util.compare(out, inp, gs, 1e-5, mode)
+        nvec = gs * (2 if dtype != torch.float32 else 4) // 16
+        if 256 <= nvec <= 1024:
+            assert plan["path"] == g.PATH_WIDE_CLUSTER, (rows, width, gs, plan)
 
 
 def test_strided_views_and_canaries():
