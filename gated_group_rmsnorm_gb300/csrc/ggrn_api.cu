@@ -731,9 +731,11 @@ int launch(const Args& a, const Plan& plan, cudaStream_t s) {
   SlotTable* table = nullptr;
   std::unique_lock<std::mutex> hold;  // held from the slot's choice to its event
   int slot = -1;
-  if (p.path == kStream) {
+  if (p.path == kStream || p.path == kWideCluster) {
     k.fault = fault_word();
     if (!k.fault) return GGRN_ERR_CUDA;
+  }
+  if (p.path == kStream) {
     // A graph replays its launches with the parameters they were recorded
     // with, the claim epoch included: recorded launches take the static
     // schedule.

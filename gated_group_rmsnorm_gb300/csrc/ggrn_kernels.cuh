@@ -824,22 +824,63 @@ __global__ void __launch_bounds__(256) k_scalar(const KParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Launch of the kernel a plan names, for one element type.
+// Shared-memory barriers (mbarrier) and bounded waits, used by the cluster
+// kernel below and by the streaming family (ggrn_stream.cuh).
 // ---------------------------------------------------------------------------
-// The streaming family lives in ggrn_stream.cuh.
+// At most kWaitLimit polls, each suspending for at most ~kWaitHintNs: a wait
+// gives up after about a second (a normal wait lasts microseconds).
+constexpr uint32_t kWaitLimit = 1u << 20;
+constexpr uint32_t kWaitHintNs = 1000;
+// Fault bits of the device status word.
+constexpr uint32_t kFaultConsumerWait = 1u;
+constexpr uint32_t kFaultProducerWait = 2u;
+constexpr uint32_t kFaultDrainWait = 4u;
+constexpr uint32_t kFaultClaim = 8u;
+constexpr uint32_t kFaultClusterWait = 32u;
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // k_wide_cluster: one cluster of CN CTAs per group (a few wide groups: a
 // batch-1 decode step of a norm with one wide group).  CTA `rank` takes
 // vectors [rank * per, (rank + 1) * per) of the group, one per thread
 // (per = p.cluster_vecs; CTAs x warps per CTA <= 32).  Lane r of each warp
-// stores the warp's partial sum of squares into slot rank * warps + warp of
-// CTA r's shared memory (distributed shared memory); after one cluster
-// barrier every warp of every CTA adds the 32 slots with the same butterfly,
-// so all CTAs get the same bits and no CTA touches another after the
-// barrier.  A relaxed cluster arrive at entry, waited on just before the
-// first remote store, makes sure every CTA of the cluster is running before
-// its shared memory is written.  Cluster barriers are hardware barriers over
-// co-scheduled CTAs: every CTA reaches each of them.
+// sends the warp's partial sum of squares to slot rank * warps + warp of CTA
+// r with an asynchronous remote store (st.async) that also counts its 4 bytes
+// on CTA r's mbarrier; each CTA waits on its own mbarrier for all the
+// cluster's slots, then every warp adds the 32 slots with the same butterfly,
+// so all CTAs get the same bits.  A CTA's shared memory receives nothing
+// after its wait completes, so it may exit then.  The mbarrier is set up
+// before a relaxed cluster arrive at entry, which every CTA waits on before
+// its first remote store: each target is running and its mbarrier is
+// initialised when the stores arrive.  The waits are bounded.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -852,16 +893,19 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Store v at the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ void st_cluster_f32(float* own_addr, uint32_t rank, float v) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(own_addr));
+// Map a shared-memory address of this CTA to the same location in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t own, uint32_t rank) {
   uint32_t m;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(m), "f"(v) : "memory");
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(own), "r"(rank));
+  return m;
+}
+// Store v at `addr` in another CTA of the cluster, counting 4 bytes on the
+// mbarrier `bar` of that CTA (both addresses mapped with map_to_rank).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "f"(v), "r"(bar)
+               : "memory");
 }
 
 template <typename T, int MODE>
@@ -869,14 +913,22 @@ __global__ void __launch_bounds__(512) k_wide_cluster(const KParams p) {
   constexpr int E = Elem<T>::E;
   // slot r * nwarps + w: warp w of CTA r's partial sum (CTAs x warps <= 32)
   __shared__ float partials[32];
-  cluster_arrive_relaxed();  // this CTA is running (waited on before the pushes)
-  pdl_wait();
-  pdl_launch_dependents();
+  __shared__ __align__(8) unsigned long long full;  // every slot has landed
   const int CN = p.cluster_ctas;  // CTAs per cluster (the launch's cluster size)
-  const uint32_t rank = cluster_ctarank();
-  const int64_t item = blockIdx.x / CN;  // the group of this cluster
   const int tid = threadIdx.x;
   const int nwarps = blockDim.x >> 5;
+  const int nslots = CN * nwarps;
+  const uint32_t bar = smem_u32(&full);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_expect_tx(bar, static_cast<uint32_t>(nslots) * 4u);  // the one arrival, and the bytes
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster_arrive_relaxed();  // waited on before the first remote store
+  pdl_wait();
+  pdl_launch_dependents();
+  const uint32_t rank = cluster_ctarank();
+  const int64_t item = blockIdx.x / CN;  // the group of this cluster
   const int64_t row = div_by(item, p.groups, p.div_magic);
   const int64_t g = item - row * p.groups;
   const int64_t col0 = g * p.gs;
@@ -909,14 +961,19 @@ __global__ void __launch_bounds__(512) k_wide_cluster(const KParams p) {
   float ss = c0 + c1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  // every warp pushes its partial to its slot in every CTA of the cluster
-  // (lane r stores to CTA r)
+  // every warp sends its partial to its slot in every CTA of the cluster
+  // (lane r to CTA r)
   const int warp = tid >> 5, lane = tid & 31;
-  const int nslots = CN * nwarps;
-  cluster_wait();  // every CTA of the cluster has started
-  if (lane < CN)
-    st_cluster_f32(&partials[static_cast<int>(rank) * nwarps + warp], static_cast<uint32_t>(lane), ss);
-  cluster_barrier();  // every warp's partial is in every CTA's slots
+  cluster_wait();  // every CTA of the cluster is running, its mbarrier set up
+  if (lane < CN) {
+    const uint32_t r = static_cast<uint32_t>(lane);
+    st_async_f32(map_to_rank(smem_u32(&partials[static_cast<int>(rank) * nwarps + warp]), r), ss,
+                 map_to_rank(bar, r));
+  }
+  if (!mbar_wait(bar, 0)) {
+    if (tid == 0) atomicOr(p.fault, kFaultClusterWait);
+    return;
+  }
   // a warp butterfly over the 32 slots (0 past the used ones): the same
   // operations, hence the same bits, in every warp of every CTA
   float m2 = lane < nslots ? partials[lane] : 0.0f;
@@ -937,6 +994,10 @@ __global__ void __launch_bounds__(512) k_wide_cluster(const KParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Launch of the kernel a plan names, for one element type.  (The streaming
+// family lives in ggrn_stream.cuh.)
+// ---------------------------------------------------------------------------
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s);
 

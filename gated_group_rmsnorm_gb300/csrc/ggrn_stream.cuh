@@ -54,15 +54,6 @@ __device__ __forceinline__ unsigned long long timeline_now() {
 
 namespace ggrn {
 
-// At most kWaitLimit polls, each suspending for at most ~kWaitHintNs: a wait
-// gives up after about a second (a normal wait lasts microseconds).
-constexpr uint32_t kWaitLimit = 1u << 20;
-constexpr uint32_t kWaitHintNs = 1000;
-// Fault bits of the device status word.
-constexpr uint32_t kFaultConsumerWait = 1u;
-constexpr uint32_t kFaultProducerWait = 2u;
-constexpr uint32_t kFaultDrainWait = 4u;
-constexpr uint32_t kFaultClaim = 8u;
 // Attempts of one unit claim against other launches' installations.
 constexpr uint32_t kClaimTries = 4096;
 // Unit shapes: ug consecutive groups of contiguous rows (flat), ug groups
@@ -71,35 +62,6 @@ constexpr int kUnitFlat = 0;
 constexpr int kUnitChunk = 1;
 constexpr int kUnitRows = 2;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kWaitHintNs)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {

@@ -330,7 +330,9 @@ int ggrn_version(void);
  * STREAM kernels bound every wait on a shared-memory barrier; a wait that
  * runs out stops the kernel and sets a bit here: 1 = a consumer waited for
  * data, 2 = the producer waited for a free stage, 4 = the producer waited for
- * its copies to land, 8 = a unit claim of the dynamic schedule gave up.
+ * its copies to land, 8 = a unit claim of the dynamic schedule gave up;
+ * 32 = a WIDE_CLUSTER CTA waited for its cluster's partial sums (16: see
+ * ggrn_norm_outproj).
  * Nonzero means the outputs of some call are incomplete.  Synchronises the device, writes the word to *flags and, when
  * `clear` is nonzero, resets it.  Returns GGRN_OK, GGRN_ERR_ARG (flags NULL)
  * or GGRN_ERR_CUDA.
