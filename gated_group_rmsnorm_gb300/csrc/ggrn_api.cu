@@ -426,13 +426,13 @@ int plan_scalar(const Args& a, Plan* p) {
 // ring stages (2..max_stages) for stage slots of `stage_bytes`, staging the
 // weight (`wb` bytes) when it is a 16-byte multiple and leaves room for the
 // ring.  False when not even two stages fit.
-bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t max_stages, int* cps, int* ns,
-                 int64_t* wstage) {
+bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t wpad, int64_t max_stages, int* cps,
+                 int* ns, int64_t* wstage) {
   *cps = 0;
   *ns = 0;
   *wstage = 0;
   for (int staged = 1; staged >= 0 && *ns < 2; --staged) {
-    const int64_t warea = staged ? ceil_div(wb, 128) * 128 : 0;
+    const int64_t warea = staged ? ceil_div(wb + wpad, 128) * 128 : 0;
     if (staged && (wb % 16 != 0 || wb > kStreamMaxWeightBytes)) continue;
     for (int c = 2; c >= 1; --c) {
       const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 256;
@@ -551,10 +551,16 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   // The weight is staged in shared memory once per CTA when its bytes are a
   // 16-byte multiple and it leaves room for the ring.
   const int64_t wb = a.mode == kMamba2 ? a.width * 4 : a.gs * es;
+  // MAMBA2 consumers read the staged weight for every slot of a team, also
+  // the slots past the last item's vectors (their results are not stored),
+  // up to (vpl * lanes - nvec) vectors of f32 columns beyond the row's end:
+  // the weight area is that much longer
+  const int64_t wpad = a.mode == kMamba2 ? (int64_t{vpl} * lanes - nvec) * se * 4 : 0;
   int cps, ns;
   int64_t wstage;
-  if (!stream_smem(stage_bytes, wb, max_stages, &cps, &ns, &wstage))
+  if (!stream_smem(stage_bytes, wb, wpad, max_stages, &cps, &ns, &wstage))
     return GGRN_ERR_UNSUPPORTED;
+  const int64_t warea = wstage ? ceil_div(wstage + wpad, 128) * 128 : 0;
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
   // Automatic selection streams only with enough units per CTA slot: below
   // that the ring's fill and drain cost more than the register-resident TEAM
@@ -593,11 +599,18 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->grid_static = ceil_div(units, per_cta);
   p->block = (W + 1) * 32;
   p->w_smem_bytes = static_cast<uint32_t>(wstage);
-  // ring, weight, barriers full/empty/weight, unit of each stage
-  p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes +
-                             ceil_div(wstage, 128) * 128 + 8 * (2 * ns + 2) + 8 * ns);
+  p->w_area_bytes = static_cast<uint32_t>(warea);
+  // ring, weight, a 16-byte zero block, barriers full/empty/weight/permute,
+  // unit of each stage
+  p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes + warea + 16 +
+                             8 * (2 * ns + 2) + 8 * ns);
   p->div_magic = mode == 1 ? div_magic(units, upr) : 0;
   p->div_magic2 = div_magic(total, gpr);
+  // row units: a group's row within its unit is floor(gl / gpr) for gl < ug;
+  // one multiply-high gives it exactly while ug * gpr < 2^32 (div_small)
+  p->groups_magic = (mode == 2 && gpr >= 2 && ug * gpr < (int64_t{1} << 32))
+                        ? static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(gpr) + 1)
+                        : 0;
   // Teams of 4 lanes, 8 to a warp: an 8-lane phase of a shared-memory load
   // holds two teams, each reading 4 consecutive 16-byte slots of its item.
   // Consecutive items start d slots apart (mod the 8 slots of a 128-byte
@@ -861,6 +874,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.gs_magic = p.gs_magic;
   k.div_magic = p.div_magic;
   k.div_magic2 = p.div_magic2;
+  k.groups_magic = p.groups_magic;
   k.units = p.items;
   k.units_per_row = p.units_per_row;
   k.total_groups = p.total_groups;
@@ -868,6 +882,7 @@ KParams make_params(const Args& a, const Plan& p) {
   k.stages = p.stages;
   k.stage_bytes = p.stage_bytes;
   k.w_smem_bytes = p.w_smem_bytes;
+  k.w_area_bytes = p.w_area_bytes;
   k.ug = p.ug;
   k.unit_mode = p.unit_mode;
   k.rows_per_unit = p.rows_per_unit;

@@ -57,6 +57,7 @@ struct Plan {
   int stages = 0;
   uint32_t stage_bytes = 0;    // one tensor's chunk slot, 128-byte aligned
   uint32_t w_smem_bytes = 0;   // weight staged in shared memory (0: read from global)
+  uint32_t w_area_bytes = 0;   // its shared-memory area (128-byte multiple, past-the-end slack)
   int ug = 0;                  // groups per unit
   int64_t units_per_row = 0;   // chunk units per row
   int64_t total_groups = 0;
@@ -66,6 +67,7 @@ struct Plan {
   int head_size = 0;
   int team_map = kTeamsInOrder;
   uint64_t div_magic2 = 0;     // magic for floor(group / groups_per_row)
+  uint32_t groups_magic = 0;   // STREAM row units: floor(2^32 / groups) + 1, or 0 (see div_small)
   int ctas_per_sm = 0;
   // WIDE_CLUSTER: CTAs per group (the cluster) and vectors per CTA
   int cluster_ctas = 0;
@@ -105,6 +107,7 @@ struct KParams {
   int64_t total_groups;
   uint64_t div_magic;
   uint64_t div_magic2;
+  uint32_t groups_magic;
   int nvec;
   int chunk_groups;
   int warp_smem;
@@ -113,6 +116,7 @@ struct KParams {
   int stages;
   uint32_t stage_bytes;
   uint32_t w_smem_bytes;
+  uint32_t w_area_bytes;
   int ug;
   int unit_mode;
   int rows_per_unit;

@@ -175,7 +175,7 @@ __device__ __forceinline__ int64_t claim_resolve(unsigned long long* w, uint32_t
 
 // ---------------------------------------------------------------------------
 // Pieces of the streaming kernel.  Dynamic shared memory:
-// [stages][y slot | gate slot], the weight area, then the barriers
+// [stages][y slot | gate slot], the weight area, 16 bytes of zeros, then the barriers
 // full[NS], empty[NS], wbar, sbar, and the unit of each stage (int64 [NS]).
 // ---------------------------------------------------------------------------
 struct StreamCtx {
@@ -186,6 +186,7 @@ struct StreamCtx {
   uint32_t wbytes;       // 0: the weight is read from global memory
   uint32_t full0, empty0, wbar;
   uint32_t sbar;         // every consumer thread done permuting the staged weight
+  const unsigned char* zero16;  // 16 bytes of zeros (what slots outside an item read)
   int NS, W;
 };
 
@@ -199,14 +200,16 @@ __device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned cha
   c.sb = p.stage_bytes;
   c.wsm = smem + static_cast<size_t>(2) * c.NS * c.sb;
   c.wbytes = p.w_smem_bytes;
-  const uint32_t warea = (c.wbytes + 127u) & ~127u;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c.wsm + warea);
+  const uint32_t warea = p.w_area_bytes;  // the weight and its slack, 128-byte multiple
+  c.zero16 = c.wsm + warea;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(c.wsm + warea + 16);
   c.full0 = smem_u32(bars);
   c.empty0 = smem_u32(bars + c.NS);
   c.wbar = smem_u32(bars + 2 * c.NS);
   c.sbar = smem_u32(bars + 2 * c.NS + 1);
   c.unit_of = reinterpret_cast<long long*>(bars + 2 * c.NS + 2);
   if (threadIdx.x == 0) {
+    *reinterpret_cast<uint4*>(c.wsm + warea) = make_uint4(0u, 0u, 0u, 0u);
     for (int s = 0; s < c.NS; ++s) {
       mbar_init(c.full0 + 8 * s, 1);
       mbar_init(c.empty0 + 8 * s, c.W);
@@ -355,6 +358,14 @@ __device__ __forceinline__ UnitPos unit_pos(const KParams& p, int64_t u) {
   return r;
 }
 
+// floor(n / d) for a group's row within a row unit: one multiply-high by
+// magic = floor(2^32 / d) + 1, exact for every n with n * d < 2^32 (the
+// host checks that for the whole unit, else passes 0 for a plain division).
+__device__ __forceinline__ int div_small(int n, int d, uint32_t magic) {
+  if (magic != 0) return static_cast<int>(__umulhi(static_cast<unsigned>(n), magic));
+  return n / d;
+}
+
 // Output offset (elements) and weight column of group gl of a unit.
 __device__ __forceinline__ void group_place(const KParams& p, const UnitPos& up, int gl,
                                             int64_t* out_off, int64_t* wcol) {
@@ -368,7 +379,7 @@ __device__ __forceinline__ void group_place(const KParams& p, const UnitPos& up,
     *out_off = up.row * p.os + up.col + gl * gs;
     *wcol = up.col + gl * gs;
   } else {
-    const int r = gl / static_cast<int>(p.groups);  // row within the unit
+    const int r = div_small(gl, static_cast<int>(p.groups), p.groups_magic);  // row in the unit
     *wcol = (gl - r * p.groups) * gs;
     *out_off = (up.row + r) * p.os + *wcol;
   }
@@ -391,22 +402,10 @@ __device__ __forceinline__ void swap_weight_halves(unsigned char* wsm, uint32_t 
   }
 }
 
-// f32 weight of SE columns at wi (shared memory when staged; SWZ: the
-// staged copy has its halves permuted as above).
-template <int SE, bool SWZ>
+// f32 weight of SE columns at wi, as stored (shared memory when staged).
+template <int SE>
 __device__ __forceinline__ void load_w_cols(const KParams& p, const StreamCtx& c, int64_t wi,
                                             float (&wv)[SE]) {
-  if constexpr (SWZ && SE == 8) {
-    if (c.wbytes) {
-      const unsigned char* blk = c.wsm + 4 * wi;
-      const uint32_t x = 16u * ((static_cast<uint32_t>(wi) >> 5) & 1u);  // bit 2 of wi / 8
-      const float4 lo = *reinterpret_cast<const float4*>(blk + x);
-      const float4 hi = *reinterpret_cast<const float4*>(blk + (16u - x));
-      wv[0] = lo.x, wv[1] = lo.y, wv[2] = lo.z, wv[3] = lo.w;
-      wv[4] = hi.x, wv[5] = hi.y, wv[6] = hi.z, wv[7] = hi.w;
-      return;
-    }
-  }
 #pragma unroll
   for (int q = 0; q < SE; q += 4 > SE ? SE : 4) {
     if (SE >= 4) {
@@ -491,6 +490,16 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
   }
   const int nvec = static_cast<int>(Q * gs / SE);
   const int vb = static_cast<int>(gs / SE);
+  // Slots that every lane fills, and the slots wholly in an item's first or
+  // second group, from the team shapes the planner picks (launch_stream
+  // refuses any other): with 4 vectors a lane, L is the power of two at or
+  // above nvec / 4, so 2L < nvec <= 4L and a pair's split vector
+  // vb = (nvec - 1) / 2 lies in [L, 2L); the 4 x 7 pairs have 17 <= nvec <= 27
+  // and 8 <= vb <= 13.  Slot k holds vector k * L + tl.
+  constexpr int kFull = VPL == 7 ? 4 : 2;  // k < kFull: v < nvec in every lane
+  constexpr int kG0 = VPL == 7 ? 2 : 1;    // k < kG0: v < vb
+  constexpr int kG1 = VPL == 7 ? 4 : 2;    // k >= kG1: v > vb
+  constexpr bool kBranchFree = MODE == kMamba2;
   const int items_per_pass = W * TPW;
 #ifdef GGRN_TIMELINE
   unsigned long long tl_first = 0;  // kept in registers: no global access in the loop
@@ -517,7 +526,15 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     for (int pass = 0; pass * items_per_pass < nitems; ++pass) {
       const int item = pass * items_per_pass + warp * TPW + titem;
       const bool active = item < nitems;
-      const int gl = item * Q;  // first group of the item within the unit
+      // items rise with the pass: a warp with no item left is done with the unit
+      if (!__any_sync(0xffffffffu, active)) break;
+      // MAMBA2: the loop body is branch-free.  A team past the unit's items
+      // computes on the pass's first item (in bounds) and stores nothing; a
+      // slot past the item's vectors reads the zero block (y = gate = 0:
+      // nothing added to the sums) and stores nothing (prefill +1.5 %, odd
+      // span +1.2 %).  ONNX keeps branches around those slots (its 128-wide
+      // heads measured 1.5 % slower branch-free).
+      const int gl = (active ? item : pass * items_per_pass) * Q;  // first group of the item
       int64_t out_off, wcol;    // output origin and weight column of that group
       group_place(p, up, gl, &out_off, &wcol);
       const unsigned char* gy = sy + static_cast<size_t>(gl) * gs * ES;
@@ -527,7 +544,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
         const int v = k * L + tl;
-        if (active && v < nvec) {
+        const bool in = k < kFull || v < nvec;
+        if (kBranchFree) {
+          yr[k] = lds_words<NW>(in ? gy + v * SV : c.zero16);
+          gr[k] = lds_words<NW>(in ? gg + v * SV : c.zero16);
+        } else if (active && in) {
           yr[k] = lds_words<NW>(gy + v * SV);
           gr[k] = lds_words<NW>(gg + v * SV);
         } else {
@@ -558,8 +579,14 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
           sumsq2<SE / 2>(a[k] + SE / 2, h1a, h1b);
           const float h0 = h0a + h0b, h1 = h1a + h1b;
           const int v = k * L + tl;
-          s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
-          s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
+          if (k < kG0) {
+            s0 += h0 + h1;
+          } else if (k >= kG1) {
+            s1 += h0 + h1;
+          } else {
+            s0 += (v < vb) ? h0 + h1 : (v == vb ? h0 : 0.0f);
+            s1 += (v > vb) ? h0 + h1 : (v == vb ? h1 : 0.0f);
+          }
         }
       }
       if constexpr (Q == 1) s0 = c0 + c1;
@@ -572,43 +599,70 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
       const float nf1 = (Q == 2) ? normaliser(s1, p.gs_f, p.eps) : nf0;
 
       T* op = static_cast<T*>(p.out) + out_off;
+      // The staged, permuted weight (kSwz): slot k's 32-byte block starts
+      // k * L * SE columns after the lane's slot-0 block, and its halves are
+      // swapped when bit 5 of its first column is set, which is bit 5 of the
+      // slot-0 column flipped by the constant bit 5 of k * L * SE (L * SE is a
+      // multiple of 32).  wA / wB: the slot-0 block's first / second half as
+      // read.  Slots past the last item's vectors read the area's slack.
+      const unsigned char* wA = wsm;
+      const unsigned char* wB = wsm;
+      if (kSwz) {
+        const uint32_t wb0 = static_cast<uint32_t>(wcol) + static_cast<uint32_t>(tl * SE);
+        const uint32_t x0 = 16u * ((wb0 >> 5) & 1u);
+        wA = wsm + 4u * wb0 + x0;
+        wB = wsm + 4u * wb0 + (16u - x0);
+      }
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
         const int v = k * L + tl;
-        if (active && v < nvec) {
-          // normaliser of each half of the vector
-          const float nlo = (Q == 1 || v <= vb) ? nf0 : nf1;
-          const float nhi = (Q == 1 || v < vb) ? nf0 : nf1;
-          float r[SE];
-          if (MODE == kMamba2) {
-            float wv[SE];
-            load_w_cols<SE, kSwz>(p, c, wcol + v * SE, wv);
-            mamba2_out<T, SE>(a[k], nlo, nhi, wv, r);
+        const bool in = k < kFull || v < nvec;
+        if (!kBranchFree && !(active && in)) continue;
+        const int vc = in ? v : 0;  // a slot past the item reads vector 0's weights
+        // normaliser of each half of the vector, and whether each half is in
+        // the item's first group
+        const bool lo0 = Q == 1 || k < kG0 || (k < kG1 && v <= vb);
+        const bool hi0 = Q == 1 || k < kG0 || (k < kG1 && v < vb);
+        const float nlo = lo0 ? nf0 : nf1;
+        const float nhi = hi0 ? nf0 : nf1;
+        float r[SE];
+        if (MODE == kMamba2) {
+          float wv[SE];
+          if (kSwz && wbytes) {
+            const bool flip = ((k * L * SE) >> 5) & 1;
+            const float4 lo = *reinterpret_cast<const float4*>((flip ? wB : wA) + 4 * k * L * SE);
+            const float4 hi = *reinterpret_cast<const float4*>((flip ? wA : wB) + 4 * k * L * SE);
+            wv[0] = lo.x, wv[1 % SE] = lo.y, wv[2 % SE] = lo.z, wv[3 % SE] = lo.w;
+            wv[4 % SE] = hi.x, wv[5 % SE] = hi.y, wv[6 % SE] = hi.z, wv[7 % SE] = hi.w;
           } else {
-            float sc[SE], gf[SE];
-            if constexpr (Q == 1) {
-              words_to_f32<T, NW>(wbytes ? lds_words<NW>(wsm + v * SV)
-                                         : ldg_words<NW>(static_cast<const T*>(p.w) + v * SE),
-                                  sc);
-            } else {
-              // scale index restarts at each group: each half has its own offset
-              const int jlo = v * SE - (v <= vb ? 0 : static_cast<int>(gs));
-              const int jhi = v * SE + SE / 2 - (v < vb ? 0 : static_cast<int>(gs));
-              const T* wt = static_cast<const T*>(p.w);
-              words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jlo * ES)
-                                             : ldg_words<NW / 2>(wt + jlo),
-                                      sc);
-              words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jhi * ES)
-                                             : ldg_words<NW / 2>(wt + jhi),
-                                      sc + SE / 2);
-            }
-            words_to_f32<T, NW>(gr[k], gf);
-            float sgv[SE];
-            silu_vec<T, SE>(gf, sgv);
-            onnx_out<SE>(a[k], nlo, nhi, sc, sgv, r);
+            load_w_cols<SE>(p, c, wcol + vc * SE, wv);
           }
-          stg_words<NW>(op + v * SE, f32_to_words<T, NW>(r));
+          mamba2_out<T, SE>(a[k], nlo, nhi, wv, r);
+        } else {
+          float sc[SE], gf[SE];
+          if constexpr (Q == 1) {
+            words_to_f32<T, NW>(wbytes ? lds_words<NW>(wsm + vc * SV)
+                                       : ldg_words<NW>(static_cast<const T*>(p.w) + vc * SE),
+                                sc);
+          } else {
+            // scale index restarts at each group: each half has its own offset
+            const int jlo = in ? v * SE - (lo0 ? 0 : static_cast<int>(gs)) : 0;
+            const int jhi = in ? v * SE + SE / 2 - (hi0 ? 0 : static_cast<int>(gs)) : 0;
+            const T* wt = static_cast<const T*>(p.w);
+            words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jlo * ES)
+                                           : ldg_words<NW / 2>(wt + jlo),
+                                    sc);
+            words_to_f32<T, NW / 2>(wbytes ? lds_words<NW / 2>(wsm + jhi * ES)
+                                           : ldg_words<NW / 2>(wt + jhi),
+                                    sc + SE / 2);
+          }
+          words_to_f32<T, NW>(gr[k], gf);
+          float sgv[SE];
+          silu_vec<T, SE>(gf, sgv);
+          onnx_out<SE>(a[k], nlo, nhi, sc, sgv, r);
         }
+        const Words<NW> ow = f32_to_words<T, NW>(r);
+        if (active && in) stg_words<NW>(op + v * SE, ow);
       }
     }
     __syncwarp();
@@ -666,8 +720,18 @@ cudaError_t launch_stream_sv(const KParams& k, const Plan& p, cudaStream_t s) {
   }
 }
 
+// The team shapes k_stream's static slot ranges assume (kFull, kG0, kG1):
+// 4 vectors a lane with 2L < nvec <= 4L, or 4 lanes x 7 vectors with
+// 17 <= nvec <= 27; pairs of groups have an odd vector count.
+inline bool stream_shape_ok(const Plan& p) {
+  if (p.items_groups == 2 && p.nvec % 2 == 0) return false;
+  if (p.vpl == 7) return p.lanes == 4 && p.nvec >= 17 && p.nvec <= 27;
+  return p.vpl == 4 && p.nvec > 2 * p.lanes && p.nvec <= 4 * p.lanes;
+}
+
 template <typename T, int MODE>
 cudaError_t launch_stream(const KParams& k, const Plan& p, cudaStream_t s) {
+  if (!stream_shape_ok(p)) return cudaErrorInvalidConfiguration;
   if (p.smem_vec_bytes == 16 && p.items_groups == 2 && p.lanes == 4 && p.vpl == 7)
     return launch_stream_kernel<k_stream<T, MODE, 4, 7, 16, 2, stream_max_warps(MODE, 7)>>(k, p, s);
   if (p.vpl != 4) return cudaErrorInvalidConfiguration;

@@ -379,6 +379,20 @@ def test_plans_respect_launch_limits():
             bound = 16 if info.vec_per_lane == 7 else 17   # consumer warps + producer
             assert info.block_threads <= bound * 32, case
             assert info.smem_bytes > 0, case
+            # the team shapes whose slot ranges the streaming consumers take
+            # as given (slots every lane fills; slots wholly in one group of
+            # a pair): 4 vectors a lane with 2L < nvec <= 4L, or 4 lanes x 7
+            # vectors with 17 <= nvec <= 27; pairs have an odd vector count
+            se = info.elems_per_vec
+            q = 1 if gs % se == 0 else 2
+            nvec = q * gs // se
+            lanes, vpl = info.team_lanes, info.vec_per_lane
+            if q == 2:
+                assert nvec % 2 == 1, case
+            if vpl == 7:
+                assert lanes == 4 and 17 <= nvec <= 27, case
+            else:
+                assert vpl == 4 and 2 * lanes < nvec <= 4 * lanes, case
         if info.path == g.PATH_WIDE_CLUSTER:
             # whole clusters of 2..8 CTAs, one per group
             ctas = info.grid_blocks // info.items
