@@ -435,7 +435,7 @@ bool stream_smem(int64_t stage_bytes, int64_t wb, int64_t wpad, int64_t max_stag
     const int64_t warea = staged ? ceil_div(wb + wpad, 128) * 128 : 0;
     if (staged && (wb % 16 != 0 || wb > kStreamMaxWeightBytes)) continue;
     for (int c = 2; c >= 1; --c) {
-      const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 256;
+      const int64_t budget = kStreamSmemPerSM / c - 1024 - warea - 512;
       const int64_t n = std::min<int64_t>(max_stages, budget / (2 * stage_bytes));
       if (n >= 2) {
         *cps = c;
@@ -468,6 +468,8 @@ int64_t stream_head_size(int mode, int64_t mid, int Q) {
 // vectors, every unit is a 16-byte multiple, and (unless forced) there are
 // enough units per CTA slot (kStreamMinUnitsPerSlot and its variants).
 int plan_stream(const Args& a, Plan* p, bool forced) {
+  // the consumers place groups within a unit in 32-bit arithmetic
+  if (a.width >= (int64_t{1} << 30)) return GGRN_ERR_UNSUPPORTED;
   const int es = elem_size(a.dtype);
   const int64_t gbytes = a.gs * es;
   int sv = 0, Q = 1;
@@ -601,14 +603,15 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   p->w_smem_bytes = static_cast<uint32_t>(wstage);
   p->w_area_bytes = static_cast<uint32_t>(warea);
   // ring, weight, a 16-byte zero block, barriers full/empty/weight/permute,
-  // unit of each stage
+  // unit of each stage and its placement
   p->smem = static_cast<int>(2 * static_cast<int64_t>(ns) * stage_bytes + warea + 16 +
-                             8 * (2 * ns + 2) + 8 * ns);
+                             8 * (2 * ns + 2) + 8 * ns + 16 * ns);
   p->div_magic = mode == 1 ? div_magic(units, upr) : 0;
   p->div_magic2 = div_magic(total, gpr);
-  // row units: a group's row within its unit is floor(gl / gpr) for gl < ug;
-  // one multiply-high gives it exactly while ug * gpr < 2^32 (div_small)
-  p->groups_magic = (mode == 2 && gpr >= 2 && ug * gpr < (int64_t{1} << 32))
+  // a group's row past its unit's first row is floor(c / gpr) for the
+  // group's index c from that row's start, c < gpr + ug; one multiply-high
+  // gives it exactly while (gpr + ug) * gpr < 2^32 (div_small)
+  p->groups_magic = (gpr >= 2 && (gpr + ug) * gpr < (int64_t{1} << 32))
                         ? static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(gpr) + 1)
                         : 0;
   // Teams of 4 lanes, 8 to a warp: an 8-lane phase of a shared-memory load

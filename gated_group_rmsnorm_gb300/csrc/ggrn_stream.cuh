@@ -176,12 +176,24 @@ __device__ __forceinline__ int64_t claim_resolve(unsigned long long* w, uint32_t
 // ---------------------------------------------------------------------------
 // Pieces of the streaming kernel.  Dynamic shared memory:
 // [stages][y slot | gate slot], the weight area, 16 bytes of zeros, then the barriers
-// full[NS], empty[NS], wbar, sbar, and the unit of each stage (int64 [NS]).
+// full[NS], empty[NS], wbar, sbar, the unit of each stage (int64 [NS]) and
+// its placement (UnitInfo [NS]).
 // ---------------------------------------------------------------------------
+// A unit as its consumers place it, written by the producer lane beside the
+// stage's unit index: the output offset (elements) of its first group (row
+// units: of its first row), the index of that group within its row (row
+// units: 0), and the unit's group count.
+struct UnitInfo {
+  int64_t out0;
+  int32_t cg0;
+  int32_t ngroups;
+};
+
 struct StreamCtx {
   unsigned char* ring;
   unsigned char* wsm;    // staged weight (when wbytes != 0)
   long long* unit_of;    // unit in each stage; -1: no more units
+  UnitInfo* uinfo;       // placement of each stage's unit
   uint32_t sb;           // bytes of one tensor's slot (128-aligned)
   uint32_t wbytes;       // 0: the weight is read from global memory
   uint32_t full0, empty0, wbar;
@@ -208,6 +220,7 @@ __device__ __forceinline__ StreamCtx stream_setup(const KParams& p, unsigned cha
   c.wbar = smem_u32(bars + 2 * c.NS);
   c.sbar = smem_u32(bars + 2 * c.NS + 1);
   c.unit_of = reinterpret_cast<long long*>(bars + 2 * c.NS + 2);
+  c.uinfo = reinterpret_cast<UnitInfo*>(c.unit_of + c.NS);
   if (threadIdx.x == 0) {
     *reinterpret_cast<uint4*>(c.wsm + warea) = make_uint4(0u, 0u, 0u, 0u);
     for (int s = 0; s < c.NS; ++s) {
@@ -288,41 +301,62 @@ __device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx
       ++i;
       break;
     }
-    c.unit_of[s] = u;
+    // The stage's bytes are declared and its copies issued first (with the
+    // claim for the next stage): on an HBM-bound launch the ring runs nearly
+    // empty, and the copies wait for nothing else.  Then the unit's index and
+    // placement are written and the producer arrives, which completes the
+    // phase (and publishes them) once the bytes have landed.
     unsigned char* st = c.ring + static_cast<size_t>(2) * s * c.sb;
+    UnitInfo ui;
     if (p.unit_mode == kUnitRows) {
       // R whole rows, one copy per row and tensor, packed in the slot
       int64_t nr;
       const int64_t row0 = unit_span(p, u, p.rows_per_unit, p.rows, &nr);
       const uint32_t rb = static_cast<uint32_t>(p.width * ES);
-      mbar_expect_tx(full, static_cast<uint32_t>(2 * nr) * rb);
+      mbar_add_tx(full, static_cast<uint32_t>(2 * nr) * rb);
       for (int64_t r = 0; r < nr; ++r) {
         bulk_g2s(smem_u32(st + r * rb), static_cast<const T*>(p.y) + (row0 + r) * p.ys, rb, full);
         bulk_g2s(smem_u32(st + c.sb + r * rb), static_cast<const T*>(p.gate) + (row0 + r) * p.gts,
                  rb, full);
       }
+      ui.out0 = row0 * p.os;
+      ui.cg0 = 0;
+      ui.ngroups = static_cast<int32_t>(nr * p.groups);
     } else {
-      int64_t yo, go, ngroups;
+      int64_t yo, go, ngroups, g0 = 0, row = 0, cg = 0;
       if (p.unit_mode == kUnitFlat) {
-        const int64_t g0 = unit_span(p, u, p.ug, p.total_groups, &ngroups);
+        g0 = unit_span(p, u, p.ug, p.total_groups, &ngroups);
         yo = go = g0 * gs;
       } else {
-        const int64_t row = div_by(u, p.units_per_row, p.div_magic);
-        const int64_t c0 = (u - row * p.units_per_row) * p.ug * gs;
+        row = div_by(u, p.units_per_row, p.div_magic);
+        cg = (u - row * p.units_per_row) * p.ug;
+        const int64_t c0 = cg * gs;
         ngroups = p.ug;
         yo = row * p.ys + c0;
         go = row * p.gts + c0;
       }
       const uint32_t bytes = static_cast<uint32_t>(ngroups * gs * ES);
-      mbar_expect_tx(full, 2 * bytes);
+      mbar_add_tx(full, 2 * bytes);
       bulk_g2s(smem_u32(st), static_cast<const T*>(p.y) + yo, bytes, full);
       bulk_g2s(smem_u32(st + c.sb), static_cast<const T*>(p.gate) + go, bytes, full);
+      if (p.unit_mode == kUnitFlat) {
+        ui.out0 = g0 * gs;  // out rows of flat units are contiguous
+        cg = g0 - div_by(g0, p.groups, p.div_magic2) * p.groups;
+      } else {
+        ui.out0 = row * p.os + cg * gs;
+      }
+      ui.cg0 = static_cast<int32_t>(cg);
+      ui.ngroups = static_cast<int32_t>(ngroups);
     }
+    const int64_t uc = u;
     if (dyn && i + 1 >= NS) {
       pending = atomicAdd(p.sched, 1ull);  // resolved after the next empty wait
     } else {
       u += G;
     }
+    c.unit_of[s] = uc;
+    c.uinfo[s] = ui;
+    mbar_arrive(full);
   }
   if (!ok) atomicOr(p.fault, kFaultProducerWait);
   if (!claim_ok) atomicOr(p.fault, kFaultClaim);
@@ -337,52 +371,25 @@ __device__ __forceinline__ void stream_produce(const KParams& p, const StreamCtx
   if (c.wbytes && !mbar_wait(c.wbar, 0)) atomicOr(p.fault, kFaultDrainWait);
 }
 
-// A unit's first group (flattened, flat units), its group count, and its row
-// and column origin (chunk and row units).
-struct UnitPos {
-  int64_t g0, ngroups, row, col;
-};
-__device__ __forceinline__ UnitPos unit_pos(const KParams& p, int64_t u) {
-  UnitPos r{0, 0, 0, 0};
-  if (p.unit_mode == kUnitFlat) {
-    r.g0 = unit_span(p, u, p.ug, p.total_groups, &r.ngroups);
-  } else if (p.unit_mode == kUnitChunk) {
-    r.row = div_by(u, p.units_per_row, p.div_magic);
-    r.col = (u - r.row * p.units_per_row) * p.ug * p.gs;
-    r.ngroups = p.ug;
-  } else {
-    int64_t nr;
-    r.row = unit_span(p, u, p.rows_per_unit, p.rows, &nr);
-    r.ngroups = nr * p.groups;
-  }
-  return r;
-}
-
-// floor(n / d) for a group's row within a row unit: one multiply-high by
+// floor(n / d) for a group's row offset within a unit: one multiply-high by
 // magic = floor(2^32 / d) + 1, exact for every n with n * d < 2^32 (the
-// host checks that for the whole unit, else passes 0 for a plain division).
+// host checks that for every n a unit can give, else passes 0).
 __device__ __forceinline__ int div_small(int n, int d, uint32_t magic) {
   if (magic != 0) return static_cast<int>(__umulhi(static_cast<unsigned>(n), magic));
-  return n / d;
+  return d == 1 ? n : n / d;
 }
 
-// Output offset (elements) and weight column of group gl of a unit.
-__device__ __forceinline__ void group_place(const KParams& p, const UnitPos& up, int gl,
-                                            int64_t* out_off, int64_t* wcol) {
-  const int64_t gs = p.gs;
-  if (p.unit_mode == kUnitFlat) {
-    const int64_t G = up.g0 + gl;
-    *out_off = G * gs;  // flat: out rows are contiguous
-    const int64_t row = div_by(G, p.groups, p.div_magic2);
-    *wcol = (G - row * p.groups) * gs;
-  } else if (p.unit_mode == kUnitChunk) {
-    *out_off = up.row * p.os + up.col + gl * gs;
-    *wcol = up.col + gl * gs;
-  } else {
-    const int r = div_small(gl, static_cast<int>(p.groups), p.groups_magic);  // row in the unit
-    *wcol = (gl - r * p.groups) * gs;
-    *out_off = (up.row + r) * p.os + *wcol;
-  }
+// Output offset (elements) and weight column of group gl of a unit (32-bit
+// within the unit: the host streams rows of fewer than 2^30 elements).
+__device__ __forceinline__ void group_place(const KParams& p, const UnitInfo& ui, int gl,
+                                            int64_t* out_off, int* wcol) {
+  const int gs = static_cast<int>(p.gs);
+  const int groups = static_cast<int>(p.groups);
+  const int cg = ui.cg0 + gl;                          // group index from the unit's first row
+  const int r = div_small(cg, groups, p.groups_magic);  // rows past the unit's first row
+  *wcol = (cg - r * groups) * gs;  // (unused, and not computed, in ONNX flat and chunk units)
+  *out_off = p.unit_mode == kUnitRows ? ui.out0 + r * p.os + *wcol
+                                      : ui.out0 + gl * gs;  // flat and chunk: contiguous
 }
 
 // The staged f32 weight of MAMBA2 with 16-bit T is read 32 bytes (one
@@ -519,8 +526,24 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
     }
 #endif
     if (u < 0) break;
-    const UnitPos up = unit_pos(p, u);
-    const int nitems = static_cast<int>(up.ngroups / Q);
+    // ONNX flat units need only the output offset, which the unit index gives
+    // at once; reading the producer's placement instead put a dependent
+    // shared-memory load first in every stage (heads 7047 -> 7009 GB/s)
+    UnitInfo ui;
+    if constexpr (MODE == kOnnx) {
+      if (p.unit_mode == kUnitFlat) {
+        int64_t ng;
+        const int64_t g0 = unit_span(p, u, p.ug, p.total_groups, &ng);
+        ui.out0 = g0 * p.gs;
+        ui.cg0 = 0;  // (the weight column is not used)
+        ui.ngroups = static_cast<int32_t>(ng);
+      } else {
+        ui = c.uinfo[s];
+      }
+    } else {
+      ui = c.uinfo[s];
+    }
+    const int nitems = ui.ngroups / Q;
     const unsigned char* sy = smem + static_cast<size_t>(2) * s * sb;
     const unsigned char* sg = sy + sb;
     for (int pass = 0; pass * items_per_pass < nitems; ++pass) {
@@ -535,10 +558,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_stream(const KParams p) 
       // span +1.2 %).  ONNX keeps branches around those slots (its 128-wide
       // heads measured 1.5 % slower branch-free).
       const int gl = (active ? item : pass * items_per_pass) * Q;  // first group of the item
-      int64_t out_off, wcol;    // output origin and weight column of that group
-      group_place(p, up, gl, &out_off, &wcol);
-      const unsigned char* gy = sy + static_cast<size_t>(gl) * gs * ES;
-      const unsigned char* gg = sg + static_cast<size_t>(gl) * gs * ES;
+      int64_t out_off;  // output origin of that group
+      int wcol;         // and its weight column
+      group_place(p, ui, gl, &out_off, &wcol);
+      const unsigned char* gy = sy + gl * static_cast<int>(gs) * ES;
+      const unsigned char* gg = sg + gl * static_cast<int>(gs) * ES;
 
       Words<NW> yr[VPL], gr[VPL];
 #pragma unroll
