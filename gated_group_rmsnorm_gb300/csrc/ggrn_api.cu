@@ -488,16 +488,18 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   int vpl = 4;
   // Consumer warps and ring depth by team width, from a sweep of 4-16 warps,
   // 1-2 CTAs per SM and 2-4 stages over groups of 64..960 elements (claimed
-  // units): one group per warp (32-lane teams) runs best with 16 warps and
-  // three stages in one CTA per SM (+0.7 % at 960); narrow groups (teams of
-  // at most 4 lanes) with 6 warps and three stages, two CTAs per SM (+1.5 to
-  // 1.9 % at 64 and 128); 8- and 16-lane teams with 8 warps and two stages.
+  // units): narrow groups (teams of at most 4 lanes) run best with 6 warps
+  // and three stages, two CTAs per SM (+1.5 to 1.9 % at 64 and 128); 8- and
+  // 16-lane teams with 8 warps and two stages.  One group per warp (32-lane
+  // teams) ran best with 16 warps and three stages in one CTA per SM until
+  // the consumer loop lost a fifth of its instructions; since then 8 warps
+  // and two stages in each of two CTAs per SM (two independent rings, the
+  // weight staged in each) measure faster on the 960-wide prefill groups:
+  // 6271 -> 6305 GB/s at 4096 rows, 6633 -> 6767 at 8192, 7125 -> 7225 at
+  // 32768 (alternating runs on one box; not staging the weight: 6056 at 4096).
   int target_warps = kStreamWarps;
   int64_t max_stages = kStreamMaxStages;
-  if (Q == 1 && lanes == 32) {
-    target_warps = 16;
-    max_stages = 3;
-  } else if (Q == 1 && lanes <= 4) {
+  if (Q == 1 && lanes <= 4) {
     target_warps = 6;
     max_stages = 3;
   }

@@ -118,14 +118,14 @@ def _plan(rows, width, gs, dtype, mode=0, ys=None, off=0, path=0):
 
 
 def test_plan_selects_families():
-    # Mamba-2 prefill 4096x7680, group 960: streamed, two rows (16 groups) per
-    # unit after a first unit of one row for each of the 152 CTA slots, one
-    # warp per group (32 lanes x 4 vectors of 16 bytes), 16 consumer warps +
-    # 1 producer warp, one CTA on each of 152 SMs claiming units
+    # Mamba-2 prefill 4096x7680, group 960: streamed, one row (8 groups) per
+    # unit after a first unit of half a row for each of the 304 CTA slots,
+    # one warp per group (32 lanes x 4 vectors of 16 bytes), 8 consumer warps
+    # + 1 producer warp, two CTAs on each of 152 SMs claiming units
     p = _plan(4096, 7680, 960, 2)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads) == \
-        (g.PATH_STREAM, 32, 4, 152 + (4096 - 152) // 2, 17 * 32)
-    assert p.grid_blocks == 152
+        (g.PATH_STREAM, 32, 4, 304 + (4096 * 8 - 304 * 4) // 8, 9 * 32)
+    assert p.grid_blocks == 304
     # the same shape on the register-resident family: one warp per group
     p = _plan(4096, 7680, 960, 2, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 32, 4, 32768)
@@ -318,8 +318,8 @@ def test_host_pipeline_rejects_before_enqueueing():
 def test_stream_short_first_units():
     """A short first unit per CTA slot once the rest fills a full unit per
     slot: units = slots + ceil((n - slots * head) / unit)."""
-    # prefill (flat, 152 slots, head 8 of 16 groups, 8 groups a row)
-    for rows, units in ((455, -(-455 * 8 // 16)), (456, 152 + 152), (457, 152 + -(-(457 * 8 - 1216) // 16))):
+    # prefill (flat, 304 slots, head 4 of 8 groups, 8 groups a row)
+    for rows, units in ((455, 455), (456, 304 + 304), (457, 304 + -(-(457 * 8 - 1216) // 8))):
         assert _plan(rows, 7680, 960, 2, path=g.PATH_STREAM).items == units, rows
     # odd span (rows of 48 groups, 152 slots, head 4 of 5 rows)
     for rows, units in ((1367, -(-1367 // 5)), (1368, 152 + 152), (1369, 152 + 153)):
@@ -332,8 +332,9 @@ def test_stream_short_first_units():
 def test_stream_threshold_by_team_layout():
     """Automatic selection streams from 12 units per CTA slot for 32-lane
     teams, 36 for teams of at most 4 lanes and 8 for paired 4 x 7 teams."""
-    # prefill: 2-row units, 152 slots -> from 12 * 152 units (3647 rows)
-    assert _plan(3645, 7680, 960, 2).path != g.PATH_STREAM
+    # prefill: 1-row units, 304 slots -> from 12 * 304 units (3648 rows;
+    # counted before the short first units are cut)
+    assert _plan(3647, 7680, 960, 2).path != g.PATH_STREAM
     assert _plan(3648, 7680, 960, 2).path == g.PATH_STREAM
     # 128-wide fp16 heads: units of 48 of the 32 heads a row, 304 slots ->
     # from 36 * 304 units (16415 rows)
