@@ -505,12 +505,16 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   }
   if (Q == 2 && nvec > 16 && nvec <= 28) {
     // a pair of 17..28 vectors (25 for the 100-wide bf16 odd span): 4 lanes x
-    // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25); as many
-    // consumer warps as the registers allow (one CTA per SM) hide the longer
-    // per-lane latency (odd span: 15 warps 6.42 TB/s, 12 warps 6.03)
+    // 7 vectors leave fewer slots idle than 8 x 4 (28 vs 32 for 25).  With
+    // the earlier, longer consumer loop as many consumer warps as the
+    // registers allow in one CTA per SM hid the per-lane latency best (odd
+    // span: 15 warps 6.42 TB/s, 12 warps 6.03); with the current one, 6
+    // warps in each of two CTAs per SM (two rings of two-row units) measure
+    // faster: 7101 -> 7148 GB/s at 65536 rows, 6559 -> 6718 at 16384
+    // (alternating runs on one box)
     lanes = 4;
     vpl = 7;
-    target_warps = stream_max_warps(a.mode, vpl);
+    target_warps = 6;
   }
   const int wmax = stream_max_warps(a.mode, vpl);
   const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass

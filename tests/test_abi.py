@@ -150,12 +150,12 @@ def test_plan_selects_families():
     assert (p.path, p.block_threads, p.vec_per_lane) == (g.PATH_WIDE, 128, 2)
     # odd span 100 (200 bytes, an odd number of 8-byte halves) at row stride
     # 9664: streamed in pairs of groups (25 whole 16-byte vectors) by teams of
-    # 4 lanes x 7 vectors; units of 5 whole rows (15 consumer warps x 8 teams
-    # x 2 groups = 240 groups) after a first unit of 4 rows for each CTA
-    # slot, one CTA per SM
+    # 4 lanes x 7 vectors; units of 2 whole rows (6 consumer warps x 8 teams
+    # x 2 groups = 96 groups) after a first unit of 1 row for each of the
+    # 304 CTA slots, two CTAs per SM
     p = _plan(65536, 4800, 100, 2, ys=9664)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items, p.block_threads, p.grid_blocks) == \
-        (g.PATH_STREAM, 4, 7, 152 + -(-(65536 - 152 * 4) // 5), 16 * 32, 152)
+        (g.PATH_STREAM, 4, 7, 304 + -(-(65536 - 304 * 1) // 2), 7 * 32, 304)
     # register-resident teams of 8 lanes x 4 vectors, 24 pairs per row
     p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_TEAM)
     assert (p.path, p.team_lanes, p.vec_per_lane, p.items) == (g.PATH_TEAM, 8, 4, 24 * 65536)
@@ -321,8 +321,8 @@ def test_stream_short_first_units():
     # prefill (flat, 304 slots, head 4 of 8 groups, 8 groups a row)
     for rows, units in ((455, 455), (456, 304 + 304), (457, 304 + -(-(457 * 8 - 1216) // 8))):
         assert _plan(rows, 7680, 960, 2, path=g.PATH_STREAM).items == units, rows
-    # odd span (rows of 48 groups, 152 slots, head 4 of 5 rows)
-    for rows, units in ((1367, -(-1367 // 5)), (1368, 152 + 152), (1369, 152 + 153)):
+    # odd span (rows of 48 groups, 304 slots, head 1 of 2 rows)
+    for rows, units in ((911, 456), (912, 304 + 304), (913, 304 + 305)):
         assert _plan(rows, 4800, 100, 2, ys=9664, path=g.PATH_STREAM).items == units, rows
     # chunk units (part of a row each) keep one size
     p = _plan(4096, 3 * 4096, 4096 // 4, 2, ys=4 * 4096, path=g.PATH_STREAM)
@@ -340,9 +340,9 @@ def test_stream_threshold_by_team_layout():
     # from 36 * 304 units (16415 rows)
     assert _plan(16413, 4096, 128, 1, mode=1).path == g.PATH_TEAM
     assert _plan(16416, 4096, 128, 1, mode=1).path == g.PATH_STREAM
-    # odd span: 5-row units, 152 slots -> from 8 * 152 units (6076 rows)
-    assert _plan(6075, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
-    assert _plan(6080, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
+    # odd span: 2-row units, 304 slots -> from 8 * 304 units (4863 rows)
+    assert _plan(4862, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
+    assert _plan(4863, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
 
 
 def test_plans_respect_launch_limits():
