@@ -327,7 +327,8 @@ def _decode_numbers(g, device) -> dict:
                 round(max(gl_dev, gl_wall) / (21 * (n_calls // 21)), 3),
             "lone_group_path": plan_lone["path_name"],
             "note": "max(device time, host wall time) per call over back-to-back calls; "
-                    "DecodeGraph is for chains (a 1-call graph costs more than the eager call)"}
+                    "DecodeGraph of one call launches it directly (a graph of one small "
+                    "kernel costs more to launch than the kernel)"}
 
 
 def _outproj_numbers(g, device, steps: int, d_models=(3840, 7680)) -> dict:

@@ -467,7 +467,8 @@ class DecodeGraph:
     ``calls``: list of dicts with the tensors and arguments of ``forward``
     (``y``, ``gate``, ``w``, ``out``, ``group_size``, ``eps``, ``mode``).  The
     tensors are baked into the graph: keep them alive and refill them in
-    place between replays.
+    place between replays.  A chain of one call is launched directly on each
+    replay (a graph of one small kernel costs more to launch than the kernel).
     """
 
     def __init__(self, calls: list[dict]):

@@ -310,8 +310,12 @@ typedef struct {
  *   Buffers are baked into the graph: the caller keeps them alive and
  *   refills them in place between replays.  *graph receives an opaque
  *   handle.  Host memory is allocated for the handle and the graph; no
- *   device memory is allocated by this library.
- * ggrn_graph_launch: one cudaGraphLaunch of the chain on `cuda_stream`.
+ *   device memory is allocated by this library.  A chain of one call is not
+ *   captured: the handle keeps the call, and each launch issues it as
+ *   ggrn_forward would (a graph of one small kernel costs more to launch
+ *   than the kernel itself).
+ * ggrn_graph_launch: one cudaGraphLaunch of the chain on `cuda_stream` (one
+ *   call: that call's launch on `cuda_stream`).
  * ggrn_graph_destroy: frees the handle (NULL is a no-op).  The caller must
  *   make sure no launch of it is still running on the GPU.
  */
