@@ -127,8 +127,9 @@ constexpr int64_t kStreamSmemPerSM = 226 * 1024;  // shared memory the CTAs of o
 // Ring stages (at most; the shared-memory budget may allow fewer).
 constexpr int64_t kStreamMaxStages = 2;
 constexpr int64_t kStreamMinUnitsPerSlot = 12;        // units per CTA slot to stream (see plan_stream)
+constexpr int64_t kStreamMinUnitsPerSlot32 = 6;       // 32-lane teams, one group each
 constexpr int64_t kStreamMinUnitsPerSlotNarrow = 36;  // teams of at most 4 lanes, one group each
-constexpr int64_t kStreamMinUnitsPerSlotPaired = 8;   // paired 4 x 7 teams
+constexpr int64_t kStreamMinUnitsPerSlotPaired = 3;   // paired 4 x 7 teams
 constexpr int64_t kStreamMaxWeightBytes = 64 * 1024;
 
 int elem_size(int dtype) { return dtype == kF32 ? 4 : 2; }
@@ -572,13 +573,16 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
   // Automatic selection streams only with enough units per CTA slot: below
   // that the ring's fill and drain cost more than the register-resident TEAM
-  // kernel loses.  Measured crossovers (TEAM vs STREAM, GB/s): 960-wide
-  // prefill groups, 32-lane teams, 12 per slot (3072 rows 5824 vs 5525, 4096
-  // rows 6068 vs 6101); 128-wide fp16 heads, 4-lane teams, 36 per slot (8192
-  // rows 6355 vs 6248, 16384 rows 6790 vs 6800, 24576 rows 6923 vs 7002);
-  // the odd span's paired 4 x 7 teams, 8 per slot (5120 rows 4799 vs 4772,
-  // 6144 rows 4989 vs 5025, 8192 rows 5156 vs 5398).
+  // kernel loses.  Measured crossovers (TEAM vs STREAM, GB/s, forced and
+  // automatic sweeps on one box): 960-wide prefill groups, 32-lane teams in
+  // two CTAs per SM, 6 per slot (1536 rows 4926 vs 4828, 1824 rows 5280 vs
+  // 5336, 2128 rows 5396 vs 5520, 3040 rows 5786 vs 5801); 128-wide fp16
+  // heads, 4-lane teams, 36 per slot (8192 rows 6355 vs 6248, 16384 rows
+  // 6790 vs 6800, 24576 rows 6923 vs 7002); the odd span's paired 4 x 7
+  // teams in two CTAs per SM, 3 per slot (1520 rows 4017 vs 3690, 2048 rows
+  // 4057 vs 4417, 4096 rows 4730 vs 5390); other team widths 12 per slot.
   int64_t min_per_slot = kStreamMinUnitsPerSlot;
+  if (Q == 1 && lanes == 32) min_per_slot = kStreamMinUnitsPerSlot32;
   if (Q == 1 && lanes <= 4) min_per_slot = kStreamMinUnitsPerSlotNarrow;
   if (Q == 2 && vpl == 7) min_per_slot = kStreamMinUnitsPerSlotPaired;
   if (!forced && units < min_per_slot * gmax) return GGRN_ERR_UNSUPPORTED;

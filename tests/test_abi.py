@@ -330,19 +330,19 @@ def test_stream_short_first_units():
 
 
 def test_stream_threshold_by_team_layout():
-    """Automatic selection streams from 12 units per CTA slot for 32-lane
-    teams, 36 for teams of at most 4 lanes and 8 for paired 4 x 7 teams."""
-    # prefill: 1-row units, 304 slots -> from 12 * 304 units (3648 rows;
+    """Automatic selection streams from 6 units per CTA slot for 32-lane
+    teams, 36 for teams of at most 4 lanes and 3 for paired 4 x 7 teams."""
+    # prefill: 1-row units, 304 slots -> from 6 * 304 units (1824 rows;
     # counted before the short first units are cut)
-    assert _plan(3647, 7680, 960, 2).path != g.PATH_STREAM
-    assert _plan(3648, 7680, 960, 2).path == g.PATH_STREAM
+    assert _plan(1823, 7680, 960, 2).path != g.PATH_STREAM
+    assert _plan(1824, 7680, 960, 2).path == g.PATH_STREAM
     # 128-wide fp16 heads: units of 48 of the 32 heads a row, 304 slots ->
     # from 36 * 304 units (16415 rows)
     assert _plan(16413, 4096, 128, 1, mode=1).path == g.PATH_TEAM
     assert _plan(16416, 4096, 128, 1, mode=1).path == g.PATH_STREAM
-    # odd span: 2-row units, 304 slots -> from 8 * 304 units (4863 rows)
-    assert _plan(4862, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
-    assert _plan(4863, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
+    # odd span: 2-row units, 304 slots -> from 3 * 304 units (1823 rows)
+    assert _plan(1822, 4800, 100, 2, ys=9664).path == g.PATH_TEAM
+    assert _plan(1823, 4800, 100, 2, ys=9664).path == g.PATH_STREAM
 
 
 def test_plans_respect_launch_limits():
