@@ -468,7 +468,7 @@ int64_t stream_head_size(int mode, int64_t mid, int Q) {
 // 16-byte vectors).  Eligible when an item spans 4..128 shared-memory
 // vectors, every unit is a 16-byte multiple, and (unless forced) there are
 // enough units per CTA slot (kStreamMinUnitsPerSlot and its variants).
-int plan_stream(const Args& a, Plan* p, bool forced) {
+int plan_stream(const Args& a, Plan* p, bool forced, bool one_cta = false) {
   // the consumers place groups within a unit in 32-bit arithmetic
   if (a.width >= (int64_t{1} << 30)) return GGRN_ERR_UNSUPPORTED;
   const int es = elem_size(a.dtype);
@@ -498,9 +498,15 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   // weight staged in each) measure faster on the 960-wide prefill groups:
   // 6271 -> 6305 GB/s at 4096 rows, 6633 -> 6767 at 8192, 7125 -> 7225 at
   // 32768 (alternating runs on one box; not staging the weight: 6056 at 4096).
+  // Where two such CTAs do not fit on an SM (wide rows, whose staged weight
+  // is large), the one-CTA shape is planned instead (`one_cta`, below).
   int target_warps = kStreamWarps;
   int64_t max_stages = kStreamMaxStages;
-  if (Q == 1 && lanes <= 4) {
+  const bool wide_team = Q == 1 && lanes == 32;
+  if (wide_team && one_cta) {
+    target_warps = 16;
+    max_stages = 3;
+  } else if (Q == 1 && lanes <= 4) {
     target_warps = 6;
     max_stages = 3;
   }
@@ -515,8 +521,9 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
     // (alternating runs on one box)
     lanes = 4;
     vpl = 7;
-    target_warps = 6;
+    target_warps = one_cta ? stream_max_warps(a.mode, vpl) : 6;
   }
+  const bool paired7 = vpl == 7;
   const int wmax = stream_max_warps(a.mode, vpl);
   const int64_t gpw = (32 / lanes) * Q;   // groups per warp pass
   const int64_t gpr = a.width / a.gs;
@@ -570,6 +577,9 @@ int plan_stream(const Args& a, Plan* p, bool forced) {
   if (!stream_smem(stage_bytes, wb, wpad, max_stages, &cps, &ns, &wstage))
     return GGRN_ERR_UNSUPPORTED;
   const int64_t warea = wstage ? ceil_div(wstage + wpad, 128) * 128 : 0;
+  // the two-CTA shapes of 32-lane teams and 4 x 7 pairs need both CTAs on an
+  // SM: with one, the SM would run only their 6-8 consumer warps
+  if (!one_cta && (wide_team || paired7) && cps < 2) return plan_stream(a, p, forced, true);
   const int64_t gmax = static_cast<int64_t>(sm_count()) * cps;
   // Automatic selection streams only with enough units per CTA slot: below
   // that the ring's fill and drain cost more than the register-resident TEAM
