@@ -329,6 +329,23 @@ def test_stream_short_first_units():
     assert p.items % 4096 == 0
 
 
+def test_stream_two_cta_shapes_and_fallback():
+    """32-lane teams and 4 x 7 pairs run two CTAs of 8 (6) consumer warps per
+    SM; where two do not fit (wide rows, whose staged f32 weight is large)
+    the planner takes the one-CTA warp counts instead of leaving the SM with
+    6-8 consumer warps."""
+    p = _plan(16384, 7680, 960, 2, path=g.PATH_STREAM)
+    assert (p.block_threads, p.grid_blocks) == (9 * 32, 2 * 152)
+    p = _plan(16384, 16320, 960, 2, path=g.PATH_STREAM)
+    assert (p.block_threads, p.grid_blocks) == (17 * 32, 152)
+    p = _plan(65536, 4800, 100, 2, ys=9664, path=g.PATH_STREAM)
+    assert (p.block_threads, p.grid_blocks) == (7 * 32, 2 * 152)
+    # 120 groups a row: one-row units; two CTAs of 8 warps would not fit,
+    # one CTA takes 15 consumer warps (two rows a unit)
+    p = _plan(16384, 12000, 100, 2, ys=12064, path=g.PATH_STREAM)
+    assert (p.block_threads, p.grid_blocks) == (16 * 32, 152)
+
+
 def test_stream_threshold_by_team_layout():
     """Automatic selection streams from 6 units per CTA slot for 32-lane
     teams, 36 for teams of at most 4 lanes and 3 for paired 4 x 7 teams."""
